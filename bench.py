@@ -1,0 +1,489 @@
+#!/usr/bin/env python3
+"""Throughput of the SNACK sparse layer's hot path on GB300.
+
+One step = forward (Y = X W^T), backward-input (dX = dY W) and
+backward-weight (dW at the stored entries) of every layer of the workload at
+every batch size of the workload, through the library's C ABI.  The metric
+is effective GFLOP/s, 2 * nnz * batch per SpMM, three SpMMs per (layer,
+batch).  Default workload: the GPT-2-small MLP projections 3072x768 and
+768x3072 at 95% sparsity, batch 1, 8 and 32.
+
+Timing: W warm-up steps, then K steps, each replayed from a CUDA graph of
+the step and timed with CUDA events on the launching stream; a 256 MiB
+buffer (about twice the L2) is written between steps so every step starts
+with a cold L2.  Barrier + synchronize on both sides; the max over ranks is
+reported.  Under torchrun every rank runs its own replica (weak scaling, no
+collective on the data path).
+
+Also reported: the roofline of the dominant op (metric bytes / measured
+duration against the measured HBM copy bandwidth), an end-to-end number
+through the same calls with host buffers (pinned H2D of X and dY, D2H of Y,
+dX and dW inside the timed region), the CPU oracle on the host cores on a
+bounded sample, the SM clocks sampled during the timed region, and the
+kernel launches.
+
+`--impl reference` times the CPU oracle instead (the deliberately slow
+reference arm), on the same workload and metric.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SpMM fwd+bwd GFLOP/s (2·nnz·B) and % of HBM roofline at 90–99% sparsity"
+UNIT = "GFLOP/s"
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ ranks
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29533")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Max of x over ranks (x itself at world size 1)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9 and p[1].replace(".", "").isdigit():
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows]
+        smax = max(float(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows
+                                                         if r[3].replace(".", "").isdigit())}
+
+
+# ------------------------------------------------------------------ workload
+
+def make_cases(workload_name: str, batches=None, seed: int = 0):
+    """Host-side inputs of a workload: per layer the COO triple; per batch X, dY."""
+    import workloads
+    wl = workloads.workload(workload_name, seed)
+    cases = []
+    for L in wl.layers:
+        row, col, val = L.coo()
+        acts = {B: L.activations(B) for B in (batches or wl.batches)}
+        cases.append(dict(layer=L, row=row, col=col, val=val, acts=acts))
+    return wl, cases
+
+
+def flops_per_step(cases) -> float:
+    return float(sum(3 * 2 * c["layer"].nnz * B for c in cases for B in c["acts"]))
+
+
+def metric_bytes(op: str, nnz: int, out: int, inp: int, B: int) -> int:
+    """Minimal bytes of one op: nnz*12 + the dense operands it reads / writes."""
+    if op == "fwd":
+        return nnz * 12 + 4 * B * (inp + out)
+    if op == "bwd_input":
+        return nnz * 12 + 4 * B * (out + inp)
+    return nnz * 12 + 4 * B * (inp + out)  # bwd_weight: X and dY read, dW in the 12
+
+
+def read_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "coo_spmm_sparse_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel
+    sources are unchanged since it was taken; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    for r in rec.get("entries", []):
+        if r.get("op") == kernel and r.get("workload") == workload and \
+                r.get("source_sha") == kernel_source_sha():
+            return r.get("bytes_per_launch")
+    return None
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    rank, world = dist_init("nccl")
+    dev = torch.device("cuda", local)
+    import coo_spmm_sparse_gb300 as sn
+
+    wl, cases = make_cases(args.workload, args.batches, args.seed)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        for c in cases:
+            L = c["layer"]
+            c["h"] = sn.snack_create(L.out, L.inp, c["row"], c["col"], c["val"], stream=stream)
+            c["dev"] = {}
+            for B, (X, dY) in c["acts"].items():
+                Xd = torch.from_numpy(X).to(dev)
+                dYd = torch.from_numpy(dY).to(dev)
+                c["dev"][B] = dict(X=Xd, dY=dYd,
+                                   Y=torch.empty(B, L.out, device=dev),
+                                   dX=torch.empty(B, L.inp, device=dev),
+                                   dW=torch.empty(L.nnz, device=dev))
+    torch.cuda.synchronize()
+
+    def step():
+        for c in cases:
+            for B, d in c["dev"].items():
+                sn.snack_forward(c["h"], d["X"], d["Y"], stream=stream)
+                sn.snack_backward(c["h"], d["X"], d["dY"], d["dX"], d["dW"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    torch.cuda.synchronize()
+
+    # CUDA graph of one step (the calls only launch kernels: capturable).
+    n0 = sn.snack_launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    launches_per_step = sn.snack_launch_count() - n0
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            flush.fill_(1.0)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    total_ms = reduce_max(sum(step_ms), dev)
+    fl = flops_per_step(cases)
+    value = world * fl * args.steps / (total_ms / 1e3) / 1e9
+
+    # Per-op durations (same stream, cold L2 each rep) -> dominant op, roofline.
+    ops = []
+    reps = max(5, min(50, args.steps))
+    with torch.cuda.stream(stream):
+        for c in cases:
+            L = c["layer"]
+            for B, d in c["dev"].items():
+                for op in ("fwd", "bwd_input", "bwd_weight"):
+                    ts = []
+                    for _ in range(reps):
+                        flush.fill_(1.0)
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        if op == "fwd":
+                            sn.snack_forward(c["h"], d["X"], d["Y"], stream=stream)
+                        elif op == "bwd_input":
+                            sn.snack_backward_input(c["h"], d["dY"], d["dX"], stream=stream)
+                        else:
+                            sn.snack_backward_weight(c["h"], d["X"], d["dY"], d["dW"], stream=stream)
+                        e1.record(stream)
+                        ts.append((e0, e1))
+                    torch.cuda.synchronize()
+                    us = statistics.mean(a.elapsed_time(b) for a, b in ts) * 1e3
+                    nbytes = metric_bytes(op, L.nnz, L.out, L.inp, B)
+                    ops.append(dict(op=op, layer=L.name, shape=f"{L.out}x{L.inp}", nnz=L.nnz, B=B,
+                                    us=round(us, 3), gflops=round(2 * L.nnz * B / us / 1e3, 2),
+                                    gbs=round(nbytes / us / 1e3, 1), bytes=nbytes))
+    peak, peak_kind = read_peak()
+    for o in ops:
+        o["frac"] = round(o["gbs"] / peak, 4)
+    dom = max(ops, key=lambda o: o["us"])
+    tr = recorded_traffic(f"{dom['op']}:{dom['layer']}:B{dom['B']}", args.workload)
+    roofline = {"bound": "hbm", "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
+                "frac": dom["frac"], "traffic": tr,
+                "kernel": f"{dom['op']} {dom['shape']} nnz={dom['nnz']} B={dom['B']}",
+                "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
+                "bytes": "metric bytes nnz*12 + dense operands, per launch"}
+
+    # End to end through the same calls with host buffers.
+    pinned = []
+    for c in cases:
+        for B, d in c["dev"].items():
+            pinned.append(dict(c=c, d=d, X=torch.from_numpy(c["acts"][B][0]).pin_memory(),
+                               dY=torch.from_numpy(c["acts"][B][1]).pin_memory(),
+                               Y=torch.empty(d["Y"].shape).pin_memory(),
+                               dX=torch.empty(d["dX"].shape).pin_memory(),
+                               dW=torch.empty(d["dW"].shape).pin_memory()))
+    h2d = sum(p["X"].numel() * 4 + p["dY"].numel() * 4 for p in pinned)
+    d2h = sum(p["Y"].numel() * 4 + p["dX"].numel() * 4 + p["dW"].numel() * 4 for p in pinned)
+
+    def e2e_step():
+        for p in pinned:
+            d = p["d"]
+            d["X"].copy_(p["X"], non_blocking=True)
+            d["dY"].copy_(p["dY"], non_blocking=True)
+            sn.snack_forward(p["c"]["h"], d["X"], d["Y"], stream=stream)
+            sn.snack_backward(p["c"]["h"], d["X"], d["dY"], d["dX"], d["dW"], stream=stream)
+            p["Y"].copy_(d["Y"], non_blocking=True)
+            p["dX"].copy_(d["dX"], non_blocking=True)
+            p["dW"].copy_(d["dW"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    torch.cuda.synchronize()
+    evs2 = []
+    barrier()
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            e2e_step()
+            e1.record(stream)
+            evs2.append((e0, e1))
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in evs2), dev)
+    e2e_value = world * fl * args.steps / (e2e_ms / 1e3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cases, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded uniform-random COO patterns, N(0,1) activations)",
+            "config": {"workload": describe(wl, cases), "layers": [
+                dict(name=c["layer"].name, out=c["layer"].out, inp=c["layer"].inp,
+                     sparsity=c["layer"].sparsity, nnz=c["layer"].nnz) for c in cases],
+                "batches": sorted({B for c in cases for B in c["acts"]}),
+                "ops_per_step": "fwd + fused bwd (dX, dW) per layer per batch",
+                "launch": "CUDA graph replay of the step",
+                "l2": "flushed between timed steps (256 MiB write); flush not timed",
+                "parallelism": f"{world} independent replica(s)"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h,
+                    "how": "per step: pinned H2D of X, dY; snack_forward + snack_backward "
+                           "via the C ABI (no graph); D2H of Y, dX, dW"},
+            "gpu_launches": int(launches_per_step * args.steps),
+            "launches_per_step": int(launches_per_step),
+            "clocks": clk,
+            "wall_s_timed_region": round(wall, 4),
+            "ops": ops,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def describe(wl, cases):
+    parts = [f"{c['layer'].out}x{c['layer'].inp}@{c['layer'].sparsity:g}% (nnz {c['layer'].nnz})"
+             for c in cases]
+    bs = sorted({B for c in cases for B in c["acts"]})
+    if len(parts) > 4:
+        parts = parts[:2] + [f"... {len(parts)} layers"]
+    return f"{wl.name}: " + ", ".join(parts) + f"; batch {bs}; fwd+bwd"
+
+
+# ------------------------------------------------------------------ oracle
+
+def oracle_step(prepared):
+    import oracle
+    for p in prepared:
+        L, ref = p["layer"], p["ref"]
+        for B, (X, dY) in p["acts"].items():
+            oracle.forward(L.out, L.inp, ref["row"], ref["col"], ref["val"], X)
+            oracle.backward_input(L.out, L.inp, ref["row"], ref["col"], ref["val"], dY)
+            oracle.backward_weight(L.out, L.inp, ref["row"], ref["col"], X, dY)
+
+
+def prepare_oracle(cases):
+    import oracle
+    oracle.build()
+    return [dict(layer=c["layer"], acts=c["acts"],
+                 ref=oracle.canonicalize(c["layer"].out, c["layer"].inp, c["row"], c["col"],
+                                         c["val"])) for c in cases]
+
+
+def cpu_baseline(cases, budget_s: float = 10.0):
+    """The oracle as it stands (single-threaded C, fp64 accumulation), timed on
+    whole steps of the same workload until about budget_s of CPU work."""
+    prepared = prepare_oracle(cases)
+    fl = flops_per_step(cases)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle_step(prepared)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or el / n * (n + 1) > 3 * budget_s:
+            break
+    return {"value": round(fl * n / el / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} whole step(s) of the workload, {el:.1f} s, single thread"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    wl, cases = make_cases(args.workload, args.batches, args.seed)
+    prepared = prepare_oracle(cases)
+    fl = flops_per_step(cases)
+    for _ in range(args.warmup):
+        oracle_step(prepared)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(prepared)
+    el = time.perf_counter() - t0
+    value = fl * args.steps / el / 1e9
+    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulate, f32 in/out",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": describe(wl, cases)},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} whole step(s) of the workload"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gpt2_mlp",
+                    help="gpt2_mlp (default), toy256, large90/95/99, skewed, gpt2_decoder")
+    ap.add_argument("--batches", type=lambda s: [int(x) for x in s.split(",")], default=None)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

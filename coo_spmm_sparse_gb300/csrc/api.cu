@@ -1,0 +1,415 @@
+// C ABI of the SNACK sparse layer (declarations and contracts in snack.h).
+// Host-side orchestration only: argument checks, batch slicing, kernel
+// selection and launches.  All arithmetic runs in the kernels.
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "snack_internal.cuh"
+
+struct snack_layer {
+  snack::Layer L;
+};
+
+namespace {
+
+thread_local std::string g_create_error;
+std::atomic<uint64_t> g_launches{0};
+
+snack_status fail(snack_handle h, snack_status st, const std::string &msg) {
+  if (h)
+    h->L.last_error = msg;
+  else
+    g_create_error = msg;
+  return st;
+}
+
+snack_status cuda_fail(snack_handle h, cudaError_t e, const char *what) {
+  return fail(h, e == cudaErrorMemoryAllocation ? SNACK_ERR_ALLOC : SNACK_ERR_CUDA,
+              std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The handle's device must be current: the kernels address its memory.
+snack_status check_device(snack_handle h) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaGetDevice");
+  if (dev != h->L.device)
+    return fail(h, SNACK_ERR_INVALID_ARG,
+                "device " + std::to_string(dev) + " is current but the layer lives on device " +
+                    std::to_string(h->L.device));
+  return SNACK_OK;
+}
+
+snack_status check_dense(snack_handle h, const void *p, const char *name) {
+  if (!p) return fail(h, SNACK_ERR_INVALID_ARG, std::string(name) + " is NULL");
+  if (!aligned16(p)) return fail(h, SNACK_ERR_INVALID_ARG, std::string(name) + " is not 16-byte aligned");
+  return SNACK_OK;
+}
+
+snack_status check_shape(int64_t out, int64_t in, int64_t nnz) {
+  if (out < 1 || in < 1 || out > 0x7fffffffLL || in > 0x7fffffffLL)
+    return fail(nullptr, SNACK_ERR_INVALID_ARG, "out_features and in_features must be in [1, 2^31)");
+  if (nnz < 0) return fail(nullptr, SNACK_ERR_INVALID_ARG, "nnz must be >= 0");
+  if (nnz > 0x7fffff00LL)
+    return fail(nullptr, SNACK_ERR_UNSUPPORTED, "nnz must stay below 2^31 - 256");
+  if ((uint64_t)nnz > (uint64_t)out * (uint64_t)in)
+    return fail(nullptr, SNACK_ERR_INVALID_ARG, "nnz exceeds out_features * in_features");
+  return SNACK_OK;
+}
+
+void account(snack::Layer &L) {
+  size_t b = 0;
+  b += (size_t)L.nnz_pad * 4 * 5;  // col, row, val, csc_row, csc_perm
+  b += (size_t)(L.out + 1 + L.in + 1) * 4;
+  b += (size_t)(L.csr.nseg + L.csr.nsplit + L.csc.nseg + L.csc.nsplit) * sizeof(int4);
+  b += (size_t)(L.in + L.out) * snack::kMaxSlice * 4;
+  b += (size_t)std::max(L.csr.nslots, L.csc.nslots) * snack::kMaxSlice * 4;
+  b += (size_t)std::max(L.csr.nsplit, L.csc.nsplit) * 4;
+  L.device_bytes = b;
+}
+
+snack_status finish_create(snack_layer *h, snack_status st, const std::string &err,
+                           snack_handle *out) {
+  if (st != SNACK_OK) {
+    snack::free_layer(h->L);
+    delete h;
+    return fail(nullptr, st, err);
+  }
+  account(h->L);
+  *out = h;
+  return SNACK_OK;
+}
+
+// Run the segmented SpMM over batch slices of at most 64.
+//   rows == true : Y  = X W^T   (row segments, src = X,  lines = out)
+//   rows == false: dX = dY W    (column segments, src = dY, lines = in)
+snack_status run_spmm(snack_handle h, bool rows, const float *src, float *dst, int64_t batch,
+                      cudaStream_t s) {
+  snack::Layer &L = h->L;
+  const snack::SegTable &tab = rows ? L.csr : L.csc;
+  const int64_t src_lines = rows ? L.in : L.out;  // width of the dense operand
+  const int64_t dst_lines = rows ? L.out : L.in;
+  float *ws = rows ? L.d_xt : L.d_dyt;
+  for (int64_t b0 = 0; b0 < batch; b0 += snack::kMaxSlice) {
+    const int nb = (int)std::min<int64_t>(snack::kMaxSlice, batch - b0);
+    const snack::Plan p = snack::choose_plan(tab, nb);
+    const float *op = src + b0 * src_lines;
+    if (p.bw > 1) {
+      cudaError_t e = snack::launch_transpose(op, src_lines, nb, src_lines, ws, p.bw, s);
+      if (e != cudaSuccess) return cuda_fail(h, e, "transpose launch");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+      op = ws;
+    }
+    snack::SpmmArgs a;
+    a.seg = tab.d_seg;
+    a.nseg = tab.nseg;
+    a.split = tab.d_split;
+    a.idx = rows ? L.d_col : L.d_csc_row;
+    a.val = L.d_val;
+    a.perm = rows ? nullptr : L.d_csc_perm;
+    a.src = op;
+    a.dst = dst + b0 * dst_lines;
+    a.ld = dst_lines;
+    a.nb = nb;
+    a.partial = L.d_partial;
+    a.counter = L.d_counter;
+    cudaError_t e = rows ? snack::launch_spmm_rows(p, a, s) : snack::launch_spmm_cols(p, a, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "spmm launch");
+    if (a.nseg > 0) g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  return SNACK_OK;
+}
+
+// dW over batch slices; dyt_ready: slice's dY^T already in the workspace.
+snack_status run_sddmm_slice(snack_handle h, const float *X, const float *dY, float *dW,
+                             int64_t b0, int nb, bool dyt_ready, cudaStream_t s) {
+  snack::Layer &L = h->L;
+  const snack::Plan p = snack::choose_plan(L.csr, nb);
+  const float *xt = X + b0 * L.in;
+  const float *dyt = dY + b0 * L.out;
+  if (p.bw > 1) {
+    cudaError_t e = snack::launch_transpose(xt, L.in, nb, L.in, L.d_xt, p.bw, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "transpose launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    xt = L.d_xt;
+    if (!dyt_ready) {
+      e = snack::launch_transpose(dyt, L.out, nb, L.out, L.d_dyt, p.bw, s);
+      if (e != cudaSuccess) return cuda_fail(h, e, "transpose launch");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    dyt = L.d_dyt;
+  }
+  snack::SddmmArgs a;
+  a.seg = L.csr.d_seg;
+  a.nseg = L.csr.nseg;
+  a.col = L.d_col;
+  a.xt = xt;
+  a.dyt = dyt;
+  a.dw = dW;
+  a.accumulate = b0 > 0;
+  cudaError_t e = snack::launch_sddmm(p, a, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "sddmm launch");
+  if (a.nseg > 0) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return SNACK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+snack_status snack_create(int64_t out_features, int64_t in_features, int64_t nnz,
+                          const int32_t *row, const int32_t *col, const float *val,
+                          int ptrs_on_device, void *stream, snack_handle *out) {
+  if (!out) return fail(nullptr, SNACK_ERR_INVALID_ARG, "out handle pointer is NULL");
+  snack_status st = check_shape(out_features, in_features, nnz);
+  if (st != SNACK_OK) return st;
+  if (nnz > 0 && (!row || !col))
+    return fail(nullptr, SNACK_ERR_INVALID_ARG, "row and col must not be NULL when nnz > 0");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  snack_layer *h = new (std::nothrow) snack_layer();
+  if (!h) return fail(nullptr, SNACK_ERR_ALLOC, "host allocation failed");
+  cudaError_t e = cudaGetDevice(&h->L.device);
+  if (e != cudaSuccess) {
+    delete h;
+    return fail(nullptr, SNACK_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  }
+  h->L.out = out_features;
+  h->L.in = in_features;
+  std::string err;
+  int32_t *d_row = nullptr, *d_col = nullptr;
+  float *d_val = nullptr;
+  const int32_t *urow = row, *ucol = col;
+  const float *uval = val;
+  if (!ptrs_on_device && nnz > 0) {
+    // Stage host arrays on the device.
+    if ((e = cudaMalloc(&d_row, nnz * 4)) != cudaSuccess ||
+        (e = cudaMalloc(&d_col, nnz * 4)) != cudaSuccess ||
+        (val && (e = cudaMalloc(&d_val, nnz * 4)) != cudaSuccess) ||
+        (e = cudaMemcpyAsync(d_row, row, nnz * 4, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(d_col, col, nnz * 4, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (val && (e = cudaMemcpyAsync(d_val, val, nnz * 4, cudaMemcpyHostToDevice, s)) != cudaSuccess)) {
+      cudaFree(d_row);
+      cudaFree(d_col);
+      cudaFree(d_val);
+      delete h;
+      return fail(nullptr, e == cudaErrorMemoryAllocation ? SNACK_ERR_ALLOC : SNACK_ERR_CUDA,
+                  std::string("staging input: ") + cudaGetErrorString(e));
+    }
+    urow = d_row;
+    ucol = d_col;
+    uval = d_val;
+  }
+  st = snack::build_topology(h->L, nnz, urow, ucol, uval, s, err);
+  cudaFree(d_row);
+  cudaFree(d_col);
+  cudaFree(d_val);
+  return finish_create(h, st, err, out);
+}
+
+snack_status snack_create_random(int64_t out_features, int64_t in_features, int64_t nnz,
+                                 uint64_t seed, void *stream, snack_handle *out,
+                                 int64_t *n_trials) {
+  if (!out) return fail(nullptr, SNACK_ERR_INVALID_ARG, "out handle pointer is NULL");
+  snack_status st = check_shape(out_features, in_features, nnz);
+  if (st != SNACK_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  snack_layer *h = new (std::nothrow) snack_layer();
+  if (!h) return fail(nullptr, SNACK_ERR_ALLOC, "host allocation failed");
+  cudaError_t e = cudaGetDevice(&h->L.device);
+  if (e != cudaSuccess) {
+    delete h;
+    return fail(nullptr, SNACK_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  }
+  h->L.out = out_features;
+  h->L.in = in_features;
+  std::string err;
+  int32_t *d_row = nullptr, *d_col = nullptr;
+  if ((e = cudaMalloc(&d_row, std::max<int64_t>(nnz, 1) * 4)) != cudaSuccess ||
+      (e = cudaMalloc(&d_col, std::max<int64_t>(nnz, 1) * 4)) != cudaSuccess) {
+    cudaFree(d_row);
+    delete h;
+    return fail(nullptr, SNACK_ERR_ALLOC, std::string("cudaMalloc: ") + cudaGetErrorString(e));
+  }
+  int64_t trials = 0;
+  st = snack::draw_random_cells(out_features, in_features, nnz, seed, d_row, d_col, &trials, s, err);
+  if (st == SNACK_OK) st = snack::build_topology(h->L, nnz, d_row, d_col, nullptr, s, err);
+  cudaFree(d_row);
+  cudaFree(d_col);
+  if (st == SNACK_OK && n_trials) *n_trials = trials;
+  return finish_create(h, st, err, out);
+}
+
+snack_status snack_forward(snack_handle h, const float *X, float *Y, int64_t batch, void *stream) {
+  if (!h) return fail(nullptr, SNACK_ERR_INVALID_ARG, "handle is NULL");
+  if (batch < 1) return fail(h, SNACK_ERR_INVALID_ARG, "batch must be >= 1");
+  snack_status st;
+  if ((st = check_dense(h, X, "X")) != SNACK_OK || (st = check_dense(h, Y, "Y")) != SNACK_OK ||
+      (st = check_device(h)) != SNACK_OK)
+    return st;
+  return run_spmm(h, true, X, Y, batch, static_cast<cudaStream_t>(stream));
+}
+
+snack_status snack_backward_input(snack_handle h, const float *dY, float *dX, int64_t batch,
+                                  void *stream) {
+  if (!h) return fail(nullptr, SNACK_ERR_INVALID_ARG, "handle is NULL");
+  if (batch < 1) return fail(h, SNACK_ERR_INVALID_ARG, "batch must be >= 1");
+  snack_status st;
+  if ((st = check_dense(h, dY, "dY")) != SNACK_OK || (st = check_dense(h, dX, "dX")) != SNACK_OK ||
+      (st = check_device(h)) != SNACK_OK)
+    return st;
+  return run_spmm(h, false, dY, dX, batch, static_cast<cudaStream_t>(stream));
+}
+
+snack_status snack_backward_weight(snack_handle h, const float *X, const float *dY, float *dW,
+                                   int64_t batch, void *stream) {
+  if (!h) return fail(nullptr, SNACK_ERR_INVALID_ARG, "handle is NULL");
+  if (batch < 1) return fail(h, SNACK_ERR_INVALID_ARG, "batch must be >= 1");
+  snack_status st;
+  if ((st = check_dense(h, X, "X")) != SNACK_OK || (st = check_dense(h, dY, "dY")) != SNACK_OK ||
+      (st = check_dense(h, dW, "dW")) != SNACK_OK || (st = check_device(h)) != SNACK_OK)
+    return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int64_t b0 = 0; b0 < batch; b0 += snack::kMaxSlice) {
+    const int nb = (int)std::min<int64_t>(snack::kMaxSlice, batch - b0);
+    if ((st = run_sddmm_slice(h, X, dY, dW, b0, nb, false, s)) != SNACK_OK) return st;
+  }
+  return SNACK_OK;
+}
+
+snack_status snack_backward(snack_handle h, const float *X, const float *dY, float *dX, float *dW,
+                            int64_t batch, void *stream) {
+  if (!h) return fail(nullptr, SNACK_ERR_INVALID_ARG, "handle is NULL");
+  if (batch < 1) return fail(h, SNACK_ERR_INVALID_ARG, "batch must be >= 1");
+  if (!dX && !dW) return SNACK_OK;
+  snack_status st;
+  if ((st = check_dense(h, dY, "dY")) != SNACK_OK || (st = check_device(h)) != SNACK_OK) return st;
+  if (dX && (st = check_dense(h, dX, "dX")) != SNACK_OK) return st;
+  if (dW && ((st = check_dense(h, dW, "dW")) != SNACK_OK || (st = check_dense(h, X, "X")) != SNACK_OK))
+    return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  snack::Layer &L = h->L;
+  for (int64_t b0 = 0; b0 < batch; b0 += snack::kMaxSlice) {
+    const int nb = (int)std::min<int64_t>(snack::kMaxSlice, batch - b0);
+    // One dY^T per slice serves both products when their slice widths agree
+    // (they do: the width depends on the batch slice only).
+    if (dX && (st = run_spmm(h, false, dY + b0 * L.out, dX + b0 * L.in, nb, s)) != SNACK_OK) return st;
+    if (dW && (st = run_sddmm_slice(h, X, dY, dW, b0, nb, dX != nullptr, s)) != SNACK_OK) return st;
+  }
+  return SNACK_OK;
+}
+
+snack_status snack_prune_regrow(snack_handle h, float prune_frac, uint64_t seed, void *stream,
+                                int64_t *n_pruned, int64_t *n_trials) {
+  if (!h) return fail(nullptr, SNACK_ERR_INVALID_ARG, "handle is NULL");
+  if (!(prune_frac >= 0.0f) || prune_frac > 1.0f)
+    return fail(h, SNACK_ERR_INVALID_ARG, "prune_frac must be in [0, 1]");
+  snack_status st = check_device(h);
+  if (st != SNACK_OK) return st;
+  std::string err;
+  int64_t p = 0, t = 0;
+  st = snack::prune_regrow(h->L, prune_frac, seed, &p, &t, static_cast<cudaStream_t>(stream), err);
+  if (st != SNACK_OK) return fail(h, st, err);
+  account(h->L);
+  if (n_pruned) *n_pruned = p;
+  if (n_trials) *n_trials = t;
+  return SNACK_OK;
+}
+
+snack_status snack_values(snack_handle h, float **dev_val) {
+  if (!h || !dev_val) return fail(h, SNACK_ERR_INVALID_ARG, "NULL argument");
+  *dev_val = h->L.d_val;
+  return SNACK_OK;
+}
+
+snack_status snack_export(snack_handle h, int32_t *row, int32_t *col, float *val, int ptrs_on_device,
+                          void *stream) {
+  if (!h) return fail(nullptr, SNACK_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaMemcpyKind kind = ptrs_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost;
+  const size_t bytes = (size_t)h->L.nnz * 4;
+  cudaError_t e = cudaSuccess;
+  if (bytes && row && (e = cudaMemcpyAsync(row, h->L.d_row, bytes, kind, s)) != cudaSuccess)
+    return cuda_fail(h, e, "export row");
+  if (bytes && col && (e = cudaMemcpyAsync(col, h->L.d_col, bytes, kind, s)) != cudaSuccess)
+    return cuda_fail(h, e, "export col");
+  if (bytes && val && (e = cudaMemcpyAsync(val, h->L.d_val, bytes, kind, s)) != cudaSuccess)
+    return cuda_fail(h, e, "export val");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(h, e, "export sync");
+  return SNACK_OK;
+}
+
+snack_status snack_export_segments(snack_handle h, int32_t *row_ptr, int32_t *col_ptr,
+                                   int32_t *csc_row, int32_t *csc_perm, void *stream) {
+  if (!h) return fail(nullptr, SNACK_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const snack::Layer &L = h->L;
+  cudaError_t e = cudaSuccess;
+  const auto d2h = cudaMemcpyDeviceToHost;
+  if (row_ptr && (e = cudaMemcpyAsync(row_ptr, L.d_row_ptr, (L.out + 1) * 4, d2h, s)) != cudaSuccess)
+    return cuda_fail(h, e, "export row_ptr");
+  if (col_ptr && (e = cudaMemcpyAsync(col_ptr, L.d_col_ptr, (L.in + 1) * 4, d2h, s)) != cudaSuccess)
+    return cuda_fail(h, e, "export col_ptr");
+  if (L.nnz && csc_row && (e = cudaMemcpyAsync(csc_row, L.d_csc_row, L.nnz * 4, d2h, s)) != cudaSuccess)
+    return cuda_fail(h, e, "export csc_row");
+  if (L.nnz && csc_perm && (e = cudaMemcpyAsync(csc_perm, L.d_csc_perm, L.nnz * 4, d2h, s)) != cudaSuccess)
+    return cuda_fail(h, e, "export csc_perm");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(h, e, "export sync");
+  return SNACK_OK;
+}
+
+snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_width,
+                        int32_t *lanes_per_segment, int64_t *segments) {
+  if (!h) return fail(nullptr, SNACK_ERR_INVALID_ARG, "handle is NULL");
+  if (op < 0 || op > 2 || batch < 1) return fail(h, SNACK_ERR_INVALID_ARG, "bad op or batch");
+  const snack::SegTable &t = op == 1 ? h->L.csc : h->L.csr;
+  const snack::Plan p = snack::choose_plan(t, std::min<int64_t>(batch, snack::kMaxSlice));
+  if (slice_width) *slice_width = p.bw;
+  if (lanes_per_segment) *lanes_per_segment = p.lanes;
+  if (segments) *segments = t.nseg;
+  return SNACK_OK;
+}
+
+uint64_t snack_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int64_t snack_nnz(snack_handle h) { return h ? h->L.nnz : -1; }
+int64_t snack_out_features(snack_handle h) { return h ? h->L.out : -1; }
+int64_t snack_in_features(snack_handle h) { return h ? h->L.in : -1; }
+size_t snack_device_bytes(snack_handle h) { return h ? h->L.device_bytes : 0; }
+
+const char *snack_last_error(snack_handle h) {
+  return h ? h->L.last_error.c_str() : g_create_error.c_str();
+}
+
+const char *snack_status_string(snack_status s) {
+  switch (s) {
+    case SNACK_OK: return "ok";
+    case SNACK_ERR_INVALID_ARG: return "invalid argument";
+    case SNACK_ERR_OUT_OF_RANGE: return "index out of range";
+    case SNACK_ERR_DUPLICATE: return "duplicate (row, col)";
+    case SNACK_ERR_ALLOC: return "allocation failed";
+    case SNACK_ERR_CUDA: return "CUDA error";
+    case SNACK_ERR_UNSUPPORTED: return "unsupported size";
+    case SNACK_ERR_TIMEOUT: return "bounded search gave up";
+  }
+  return "unknown status";
+}
+
+void snack_destroy(snack_handle h) {
+  if (!h) return;
+  int prev = -1;
+  const bool switched = cudaGetDevice(&prev) == cudaSuccess && prev != h->L.device &&
+                        cudaSetDevice(h->L.device) == cudaSuccess;
+  cudaDeviceSynchronize();
+  snack::free_layer(h->L);
+  if (switched) cudaSetDevice(prev);
+  delete h;
+}
+
+}  // extern "C"

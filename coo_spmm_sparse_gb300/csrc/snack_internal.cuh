@@ -1,0 +1,131 @@
+// Internal declarations of the SNACK sparse-layer library (sm_103a).
+//
+// Device data layout of one layer (all owned by the handle):
+//   col      [nnz_pad] int32   column of entry k, canonical (row, col) order
+//   row      [nnz_pad] int32   row of entry k (canonical order)
+//   val      [nnz_pad] fp32    value of entry k (canonical order)
+//   row_ptr  [out+1]   int32   CSR index pointer
+//   csc_row  [nnz_pad] int32   row of the s-th entry in (col, row) order
+//   csc_perm [nnz_pad] int32   canonical k of the s-th entry in (col, row) order
+//   col_ptr  [in+1]    int32   CSC index pointer
+//   seg_csr / seg_csc  int4    work decomposition of rows / columns into
+//                              segments {line, begin, end, split_id}
+//   split_csr / split_csc int4 {first_segment, parts, first_slot, 0} for
+//                              lines cut into several segments
+//   workspace                  transposed dense operand slices, split partial
+//                              sums, split counters
+// nnz_pad rounds nnz up to a multiple of 4 (plus 4) so that 16-byte vector
+// loads of the index and value streams never leave the allocation; padding
+// entries hold index 0 and value 0 and are masked out by the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/snack.h"
+
+namespace snack {
+
+constexpr int kMaxSlice = 64;  // widest batch slice one kernel launch handles
+
+struct SegTable {
+  int64_t nseg = 0;
+  int64_t nsplit = 0;
+  int64_t nslots = 0;      // partial-sum slots (sum of parts over split lines)
+  double mean_len = 0.0;   // mean entries per line
+  int64_t max_len = 0;     // longest line
+  int4 *d_seg = nullptr;   // [nseg]
+  int4 *d_split = nullptr; // [nsplit]
+};
+
+struct Layer {
+  int64_t out = 0, in = 0, nnz = 0, nnz_pad = 0;
+  int device = 0;
+  int32_t *d_col = nullptr;
+  int32_t *d_row = nullptr;
+  float *d_val = nullptr;
+  int32_t *d_row_ptr = nullptr;
+  int32_t *d_csc_row = nullptr;
+  int32_t *d_csc_perm = nullptr;
+  int32_t *d_col_ptr = nullptr;
+  SegTable csr, csc;
+  // workspace
+  float *d_xt = nullptr;       // [in][64]   transposed X slice
+  float *d_dyt = nullptr;      // [out][64]  transposed dY slice
+  float *d_partial = nullptr;  // [max(csr.nslots, csc.nslots)][64]
+  int *d_counter = nullptr;    // [max(csr.nsplit, csc.nsplit)], zero between calls
+  size_t device_bytes = 0;
+  std::string last_error;
+};
+
+// Everything a segmented SpMM / SDDMM launch needs.
+struct SpmmArgs {
+  const int4 *seg;
+  int64_t nseg;
+  const int4 *split;
+  const int32_t *idx;   // column (rows) or row (columns) index stream
+  const float *val;     // canonical values
+  const int32_t *perm;  // column-order -> canonical position (or null)
+  const float *src;     // transposed dense operand [lines_src][bw]
+  float *dst;           // dense output, element (b, line) at dst[b * ld + line]
+  int64_t ld;
+  int nb;               // valid batch rows in this slice
+  float *partial;
+  int *counter;
+};
+
+struct SddmmArgs {
+  const int4 *seg;
+  int64_t nseg;
+  const int32_t *col;
+  const float *xt;   // [in][bw]
+  const float *dyt;  // [out][bw]
+  float *dw;         // [nnz]
+  int accumulate;    // add to dw instead of overwriting (batch slices > 0)
+};
+
+// Kernel selection: batch slice width, lanes per entry group, lanes per segment.
+struct Plan {
+  int bw = 1;
+  int lanes = 32;
+};
+int slice_width(int64_t nb);
+Plan choose_plan(const SegTable &t, int64_t nb);
+int entry_lanes(int bw);
+
+// Launchers (spmm_*.cu).  Return the launch's cudaError_t.
+cudaError_t launch_spmm_rows(const Plan &p, const SpmmArgs &a, cudaStream_t s);
+cudaError_t launch_spmm_cols(const Plan &p, const SpmmArgs &a, cudaStream_t s);
+cudaError_t launch_sddmm(const Plan &p, const SddmmArgs &a, cudaStream_t s);
+// dst[c * bw + b] = b < nb ? src[b * ld + c] : 0, for c < ncols, b < bw.
+cudaError_t launch_transpose(const float *src, int64_t ld, int nb, int64_t ncols, float *dst,
+                             int bw, cudaStream_t s);
+
+// Topology (topology.cu).
+snack_status build_topology(Layer &L, int64_t nnz, const int32_t *d_row_user,
+                            const int32_t *d_col_user, const float *d_val_user,
+                            cudaStream_t s, std::string &err);
+snack_status draw_random_cells(int64_t out, int64_t in, int64_t count, uint64_t seed,
+                               int32_t *d_row, int32_t *d_col, int64_t *trials,
+                               cudaStream_t s, std::string &err);
+snack_status prune_regrow(Layer &L, float frac, uint64_t seed, int64_t *pruned,
+                          int64_t *trials, cudaStream_t s, std::string &err);
+void free_layer(Layer &L);
+
+// Device memory helper: cudaMalloc with byte accounting.
+template <typename T>
+cudaError_t dev_alloc(T **p, size_t count, size_t *acct) {
+  size_t bytes = count * sizeof(T);
+  if (bytes == 0) bytes = sizeof(T);
+  cudaError_t e = cudaMalloc(reinterpret_cast<void **>(p), bytes);
+  if (e == cudaSuccess && acct) *acct += bytes;
+  return e;
+}
+
+inline int64_t pad4(int64_t n) { return ((n + 3) / 4) * 4 + 4; }
+
+}  // namespace snack

@@ -1,0 +1,286 @@
+// Segmented SpMM / SDDMM kernels of the SNACK layer for sm_103a (CUDA cores).
+//
+// The paper's SNACK-COO kernel ("Beyond Masked Sparsity", §3.2 and Appendix F
+// "Parallel-efficiency analysis") runs a (nnz-chunk x batch-column) grid with
+// one global atomicAdd per (entry, batch column), re-reading the whole COO
+// triple once per batch column.  Here the index/value stream is read ONCE per
+// call whatever the batch:
+//
+//  * Entries are ordered by line (row for Y = X W^T and dW, column for
+//    dX = dY W) and each line is cut into segments.  A TEAM of LPS lanes owns
+//    one segment; inside a team, GROUPS of G lanes each take one entry at a
+//    time, and the G lanes of a group split the batch slice (BW floats,
+//    16-byte vectors).  Each group walks 4 consecutive entries per step from
+//    one 16-byte load of indices and one of values (aligned down to a
+//    multiple of 4 and masked at the segment ends).
+//  * The dense operand is gathered from a transposed copy (line-major,
+//    [lines][BW]) so that the BW batch values of one column are contiguous:
+//    one 32..256-byte run per entry instead of BW scattered words.
+//  * Partial sums of the groups are combined with warp shuffles; only lines
+//    split into several segments (long rows / columns) meet across warps,
+//    and they do it deterministically: each segment stores its partial, the
+//    last one to arrive (atomic ticket) adds them in segment order and
+//    writes the output, then re-arms the ticket.  No floating-point atomics.
+//  * Index and value streams bypass L1 (ld.global.nc.L1::no_allocate) so
+//    that L1 keeps the gathered dense rows.
+#pragma once
+
+#include "snack_internal.cuh"
+
+namespace snack {
+
+__device__ __forceinline__ int4 ld_stream_i4(const int32_t *p) {
+  int4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.s32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float4 ld_stream_f4(const float *p) {
+  float4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+      : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// Shape of a batch slice: each lane holds NV vectors of VEC floats.
+template <int BW, int G>
+struct SliceShape {
+  static constexpr int VEC = BW >= 4 ? 4 : BW;
+  static constexpr int NV = BW >= 4 ? BW / (4 * G) : 1;
+  static_assert(BW < 4 ? G == 1 : (BW % (4 * G) == 0), "bad slice shape");
+};
+
+template <int VEC>
+__device__ __forceinline__ void load_vec(const float *p, float (&x)[VEC]);
+
+template <>
+__device__ __forceinline__ void load_vec<4>(const float *p, float (&x)[4]) {
+  const float4 f = __ldg(reinterpret_cast<const float4 *>(p));
+  x[0] = f.x;
+  x[1] = f.y;
+  x[2] = f.z;
+  x[3] = f.w;
+}
+
+template <>
+__device__ __forceinline__ void load_vec<2>(const float *p, float (&x)[2]) {
+  const float2 f = __ldg(reinterpret_cast<const float2 *>(p));
+  x[0] = f.x;
+  x[1] = f.y;
+}
+
+template <>
+__device__ __forceinline__ void load_vec<1>(const float *p, float (&x)[1]) {
+  x[0] = __ldg(p);
+}
+
+// Lane (group 0, sub) holds batch b = v*G*VEC + sub*VEC + i.
+template <int BW, int G>
+__device__ __forceinline__ void store_line(const SpmmArgs &a, int line, int sub,
+                                           const float (&r)[SliceShape<BW, G>::NV]
+                                                           [SliceShape<BW, G>::VEC]) {
+  using S = SliceShape<BW, G>;
+#pragma unroll
+  for (int v = 0; v < S::NV; ++v)
+#pragma unroll
+    for (int i = 0; i < S::VEC; ++i) {
+      const int b = v * G * S::VEC + sub * S::VEC + i;
+      if (b < a.nb) a.dst[(int64_t)b * a.ld + line] = r[v][i];
+    }
+}
+
+// One team of LPS lanes per segment; PERM = values reached through a
+// column-order -> canonical permutation (the dX = dY W direction).
+template <int BW, int G, int LPS, bool PERM>
+__global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
+  using S = SliceShape<BW, G>;
+  constexpr int VEC = S::VEC, NV = S::NV, NPT = LPS / G;
+  static_assert(LPS % G == 0 && LPS <= 32, "bad team");
+  const int lane = threadIdx.x & 31;
+  const int tlane = lane % LPS;
+  const int grp = tlane / G;
+  const int sub = tlane % G;
+  const int64_t team = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / LPS;
+  const bool active = team < a.nseg;
+  int4 sg = make_int4(0, 0, 0, -1);
+  if (active) sg = a.seg[team];
+  const int k0 = sg.y, k1 = sg.z;
+
+  float acc[NV][VEC];
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) acc[v][i] = 0.f;
+
+  const float *src = a.src + sub * VEC;
+  for (int kb = (k0 & ~3) + 4 * grp; kb < k1; kb += 4 * NPT) {
+    const int4 c4 = ld_stream_i4(a.idx + kb);
+    float w[4];
+    if constexpr (PERM) {
+      const int4 p4 = ld_stream_i4(a.perm + kb);
+      const int pp[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = (kb + e >= k0 && kb + e < k1) ? __ldg(a.val + pp[e]) : 0.f;
+    } else {
+      const float4 v4 = ld_stream_f4(a.val + kb);
+      w[0] = v4.x;
+      w[1] = v4.y;
+      w[2] = v4.z;
+      w[3] = v4.w;
+    }
+    const int cc[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (kb + e >= k0 && kb + e < k1) {
+        const float *p = src + (int64_t)cc[e] * BW;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          float x[VEC];
+          load_vec<VEC>(p + v * G * VEC, x);
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) acc[v][i] = fmaf(w[e], x[i], acc[v][i]);
+        }
+      }
+    }
+  }
+
+  // Combine the NPT groups of the team (every lane of the warp gets here).
+#pragma unroll
+  for (int off = G; off < LPS; off <<= 1)
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) acc[v][i] += __shfl_xor_sync(0xffffffffu, acc[v][i], off);
+
+  if (!active) return;
+  const int line = sg.x;
+  if (sg.w < 0) {
+    if (grp == 0) store_line<BW, G>(a, line, sub, acc);
+    return;
+  }
+
+  // Line split over several segments: park the partial, last arrival sums.
+  const int4 sp = a.split[sg.w];  // {first segment, parts, first slot, 0}
+  const int part = (int)(team - sp.x);
+  if (grp == 0) {
+    float *mine = a.partial + (int64_t)(sp.z + part) * BW + sub * VEC;
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) mine[v * G * VEC + i] = acc[v][i];
+  }
+  __threadfence();
+  const unsigned tmask = LPS == 32 ? 0xffffffffu : (((1u << LPS) - 1u) << (lane - tlane));
+  __syncwarp(tmask);
+  int last = 0;
+  if (tlane == 0) last = atomicAdd(a.counter + sg.w, 1) == sp.y - 1;
+  last = __shfl_sync(tmask, last, lane - tlane);
+  if (!last) return;
+  __threadfence();
+  if (grp == 0) {
+    float tot[NV][VEC];
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) tot[v][i] = 0.f;
+    for (int p = 0; p < sp.y; ++p) {
+      const float *q = a.partial + (int64_t)(sp.z + p) * BW + sub * VEC;
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) tot[v][i] += __ldcg(q + v * G * VEC + i);
+    }
+    store_line<BW, G>(a, line, sub, tot);
+  }
+  if (tlane == 0) a.counter[sg.w] = 0;  // re-arm for the next call
+}
+
+// dW[k] = sum_b dY[b][row_k] X[b][col_k] over the row segments; the G lanes
+// of a group each form part of the batch dot product and meet by shuffle.
+template <int BW, int G, int LPS>
+__global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
+  using S = SliceShape<BW, G>;
+  constexpr int VEC = S::VEC, NV = S::NV, NPT = LPS / G;
+  const int lane = threadIdx.x & 31;
+  const int tlane = lane % LPS;
+  const int grp = tlane / G;
+  const int sub = tlane % G;
+  const int64_t team = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / LPS;
+  if (team >= a.nseg) return;  // whole teams (and so whole groups) leave together
+  const unsigned gmask = G == 1 ? (1u << lane) : (((1u << G) - 1u) << (lane & ~(G - 1)));
+  const int4 sg = a.seg[team];
+  const int r = sg.x, k0 = sg.y, k1 = sg.z;
+
+  float dy[NV][VEC];
+  {
+    const float *p = a.dyt + (int64_t)r * BW + sub * VEC;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) load_vec<VEC>(p + v * G * VEC, dy[v]);
+  }
+  const float *xt = a.xt + sub * VEC;
+  for (int kb = (k0 & ~3) + 4 * grp; kb < k1; kb += 4 * NPT) {
+    const int4 c4 = ld_stream_i4(a.col + kb);
+    const int cc[4] = {c4.x, c4.y, c4.z, c4.w};
+    float res[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float s = 0.f;
+      if (kb + e >= k0 && kb + e < k1) {
+        const float *p = xt + (int64_t)cc[e] * BW;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          float x[VEC];
+          load_vec<VEC>(p + v * G * VEC, x);
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) s = fmaf(dy[v][i], x[i], s);
+        }
+      }
+#pragma unroll
+      for (int off = 1; off < G; off <<= 1) s += __shfl_xor_sync(gmask, s, off);
+      res[e] = s;
+    }
+    if (sub == 0) {
+      float *d = a.dw + kb;
+      if (kb >= k0 && kb + 3 < k1) {
+        float4 o = make_float4(res[0], res[1], res[2], res[3]);
+        if (a.accumulate) {
+          const float4 old = *reinterpret_cast<const float4 *>(d);
+          o.x += old.x;
+          o.y += old.y;
+          o.z += old.z;
+          o.w += old.w;
+        }
+        *reinterpret_cast<float4 *>(d) = o;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (kb + e >= k0 && kb + e < k1) d[e] = a.accumulate ? d[e] + res[e] : res[e];
+      }
+    }
+  }
+}
+
+// dst[c * BW + b] = b < nb ? src[b * ld + c] : 0  (32 columns per block).
+template <int BW>
+__global__ void __launch_bounds__(256) transpose_pad(const float *__restrict__ src, int64_t ld,
+                                                     int nb, int64_t ncols,
+                                                     float *__restrict__ dst) {
+  __shared__ float tile[BW][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int64_t c0 = (int64_t)blockIdx.x * 32;
+  for (int b = ty; b < BW; b += 8) {
+    const int64_t c = c0 + tx;
+    tile[b][tx] = (b < nb && c < ncols) ? src[(int64_t)b * ld + c] : 0.f;
+  }
+  __syncthreads();
+  for (int f = threadIdx.x; f < 32 * BW; f += 256) {
+    const int cc = f / BW, b = f % BW;
+    if (c0 + cc < ncols) dst[(c0 + cc) * BW + b] = tile[b][cc];
+  }
+}
+
+}  // namespace snack

@@ -1,0 +1,213 @@
+/*
+ * snack.h - C ABI of the SNACK truly-sparse linear layer for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The layer keeps its weight W (out_features x in_features) only as its
+ * stored nonzeros (row, col, val) and never forms a dense out x in matrix
+ * ("Beyond Masked Sparsity: SNACK Enables Truly Sparse Neural Networks on
+ * GPU", §3 and Appendix F "End-to-end sparsity").  The operations are
+ *
+ *   forward           Y  = X W^T                  (§3.1 Algorithm 1)
+ *   backward_input    dX = dY W                   (§3.4; Appendix F, W^T by
+ *                                                  swapping the index arrays)
+ *   backward_weight   dW[k] = sum_b dY[b,row_k] X[b,col_k], only at the
+ *                     stored entries              (§3.4; Appendix F)
+ *   prune_regrow      magnitude prune + uniform regrow (Appendix G, with the
+ *                     regrow draw of §3.3 Algorithm 2)
+ *
+ * Conventions used by every call:
+ *   - Indices are 0-based int32.  Stored entries are kept in CANONICAL ORDER:
+ *     rows ascending, columns ascending within a row.  snack_values(),
+ *     snack_export() and the dW output of the backward calls use that order.
+ *   - X is [batch][in_features], Y and dY are [batch][out_features], dX is
+ *     [batch][in_features]: dense, row-major, contiguous fp32 (the PyTorch
+ *     nn.Linear layout).  Outputs are overwritten, never accumulated into.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Compute calls are asynchronous on that stream; the caller
+ *     owns every X / Y / dY / dX / dW buffer, which must be device memory,
+ *     16-byte aligned.
+ *   - The handle owns the topology, the values and a workspace on the
+ *     device that was current at creation.  Calls must run with that device
+ *     current.  Use one handle from one stream at a time: calls on the same
+ *     handle that overlap on the GPU share its workspace and race.
+ *   - No call aborts, traps or prints.  Every call returns a snack_status;
+ *     snack_last_error() gives a one-line reason.  A call that fails leaves
+ *     the handle as it was.
+ *   - Limits: 1 <= out_features, in_features < 2^31; 0 <= nnz < 2^31 and
+ *     nnz <= out_features * in_features; batch >= 1 (any size: batches above
+ *     64 run as consecutive slices of 64).
+ */
+#ifndef SNACK_H
+#define SNACK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct snack_layer *snack_handle;
+
+typedef enum {
+  SNACK_OK = 0,
+  SNACK_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad size        */
+  SNACK_ERR_OUT_OF_RANGE = 2, /* an index outside [0,out) x [0,in)          */
+  SNACK_ERR_DUPLICATE = 3,    /* the same (row, col) stored twice           */
+  SNACK_ERR_ALLOC = 4,        /* device or host allocation failed           */
+  SNACK_ERR_CUDA = 5,         /* a CUDA runtime call failed                 */
+  SNACK_ERR_UNSUPPORTED = 6,  /* size beyond a documented limit             */
+  SNACK_ERR_TIMEOUT = 7       /* a bounded search gave up (prune/regrow)    */
+} snack_status;
+
+/*
+ * Build a layer from a COO triple given in any order (Appendix B, Table 7:
+ * the COO, CSR and CSC forms of one matrix).  The library validates the
+ * indices, sorts the entries into canonical order and builds, on the
+ * device, the row segmentation (CSR index pointer, out_features+1 entries)
+ * and the column segmentation (CSC index pointer, in_features+1 entries,
+ * plus the row index and canonical position of every entry in column
+ * order).  These are rebuilt only when the topology changes.
+ *
+ *   row, col  [nnz] int32 indices; val [nnz] fp32 values or NULL (zeros).
+ *   ptrs_on_device  1 if row/col/val are device pointers, 0 if host.
+ *   out       receives the new handle (unchanged on failure).
+ * Errors: SNACK_ERR_OUT_OF_RANGE or SNACK_ERR_DUPLICATE (no entry is summed
+ * or dropped), SNACK_ERR_INVALID_ARG, SNACK_ERR_ALLOC, SNACK_ERR_CUDA.
+ * Synchronises `stream`.
+ */
+snack_status snack_create(int64_t out_features, int64_t in_features, int64_t nnz,
+                          const int32_t *row, const int32_t *col, const float *val,
+                          int ptrs_on_device, void *stream, snack_handle *out);
+
+/*
+ * Build a layer whose nnz stored cells are drawn on the device by the
+ * uniform connection initializer (§3.3 Algorithm 2): candidate t is cell
+ * floor(x_t * out*in / 2^64) of the row-major cell numbering, where x_t is
+ * draw t of the counter-based SplitMix64 stream started at `seed` (the
+ * finaliser applied to seed + (t+1) * 0x9E3779B97F4A7C15); a candidate
+ * already drawn is rejected.  Values start at 0 (write them through
+ * snack_values()).  n_trials (may be NULL) receives the number of
+ * candidates drawn.  Synchronises `stream`.
+ */
+snack_status snack_create_random(int64_t out_features, int64_t in_features, int64_t nnz,
+                                 uint64_t seed, void *stream, snack_handle *out,
+                                 int64_t *n_trials);
+
+/*
+ * Y = X W^T (§3.1 Algorithm 1; Y^T = C, X^T = B in the paper's notation).
+ *   X [batch][in_features] in, Y [batch][out_features] out (overwritten).
+ * Asynchronous on `stream`.
+ */
+snack_status snack_forward(snack_handle h, const float *X, float *Y, int64_t batch,
+                           void *stream);
+
+/*
+ * dX = dY W, the input gradient W^T (dL/dA) of §3.4, evaluated over the
+ * column segmentation (W^T has W's support with the index arrays swapped,
+ * Appendix F).  dY [batch][out_features] in, dX [batch][in_features] out.
+ */
+snack_status snack_backward_input(snack_handle h, const float *dY, float *dX,
+                                  int64_t batch, void *stream);
+
+/*
+ * Sparse outer-product weight gradient (§3.4; Appendix F, the mini-batch sum
+ * of rank-1 terms restricted to supp(W)):
+ *   dW[k] = sum_{b<batch} dY[b][row_k] * X[b][col_k]   for each stored k,
+ * written in canonical order (nnz floats; aligned with snack_values()).
+ */
+snack_status snack_backward_weight(snack_handle h, const float *X, const float *dY,
+                                   float *dW, int64_t batch, void *stream);
+
+/*
+ * Both backward products of §3.4 in one call: dX as snack_backward_input and
+ * dW as snack_backward_weight, sharing one transposed copy of dY.  Either
+ * output may be NULL to skip it.
+ */
+snack_status snack_backward(snack_handle h, const float *X, const float *dY, float *dX,
+                            float *dW, int64_t batch, void *stream);
+
+/*
+ * One topology update (Appendix G "Sparsity schedule and DST"):
+ *  1. prune P = floor((double)prune_frac * nnz) stored entries with the
+ *     smallest |val|: ordered by the bit pattern of |val| as an unsigned
+ *     integer (-0 equals +0, NaN sorts above +inf), ties by canonical
+ *     position;
+ *  2. regrow P cells with Algorithm 2's rejection draw (the SplitMix64
+ *     stream of snack_create_random, started at `seed`), rejecting cells
+ *     held by a surviving entry or already regrown; just-pruned cells may be
+ *     drawn again;
+ *  3. survivors keep their values, regrown entries get 0; the result is put
+ *     back into canonical order and the segmentations are rebuilt.
+ * nnz is unchanged.  n_pruned / n_trials (either may be NULL) receive P and
+ * the number of candidates drawn.  Pointers previously returned by
+ * snack_values() stay valid.  Synchronises `stream`.  SNACK_ERR_TIMEOUT if
+ * 2^40 candidates do not yield P fresh cells.
+ */
+snack_status snack_prune_regrow(snack_handle h, float prune_frac, uint64_t seed,
+                                void *stream, int64_t *n_pruned, int64_t *n_trials);
+
+/*
+ * Device pointer to the nnz stored values in canonical order.  The caller
+ * may read and write them in place (e.g. an optimizer step); they stay
+ * valid until snack_destroy().
+ */
+snack_status snack_values(snack_handle h, float **dev_val);
+
+/*
+ * Copy the stored entries out in canonical order: row, col [nnz] int32 and
+ * val [nnz] fp32 (any may be NULL).  ptrs_on_device says whether the
+ * destinations are device (1) or host (0) memory.  Synchronises `stream`.
+ */
+snack_status snack_export(snack_handle h, int32_t *row, int32_t *col, float *val,
+                          int ptrs_on_device, void *stream);
+
+/*
+ * Copy the segmentations to host memory (any pointer may be NULL):
+ * row_ptr [out_features+1], col_ptr [in_features+1], csc_row [nnz],
+ * csc_perm [nnz] (canonical position of the s-th entry in column order).
+ * Synchronises `stream`.
+ */
+snack_status snack_export_segments(snack_handle h, int32_t *row_ptr, int32_t *col_ptr,
+                                   int32_t *csc_row, int32_t *csc_perm, void *stream);
+
+/*
+ * Which kernel variant a call would run: for op 0 = forward, 1 =
+ * backward_input, 2 = backward_weight and the given batch, returns the
+ * batch slice width (1, 2, 4, 8, 16, 32 or 64), the lanes that share one
+ * row (or column) segment, and the number of segments.  Pure host query.
+ */
+snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_width,
+                        int32_t *lanes_per_segment, int64_t *segments);
+
+/*
+ * Kernel launches this library has issued in the process so far (all
+ * handles, all threads).  Launches recorded into a CUDA graph count once,
+ * at capture.  For accounting and tests.
+ */
+uint64_t snack_launch_count(void);
+
+int64_t snack_nnz(snack_handle h);
+int64_t snack_out_features(snack_handle h);
+int64_t snack_in_features(snack_handle h);
+
+/* Device bytes held by the handle (topology, values, workspace). */
+size_t snack_device_bytes(snack_handle h);
+
+/*
+ * One-line text for the last failure on this handle; with h == NULL, the
+ * last failure of snack_create / snack_create_random on the calling thread.
+ * The string lives until the next call on the same handle / thread.
+ */
+const char *snack_last_error(snack_handle h);
+
+const char *snack_status_string(snack_status s);
+
+/* Free everything the handle owns (synchronises its device).  NULL is a no-op. */
+void snack_destroy(snack_handle h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SNACK_H */

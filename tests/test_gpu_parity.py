@@ -1,0 +1,326 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Forward, backward-input and backward-weight are compared element by element
+within 1e-5 * sum|terms|; canonical order, CSR/CSC segmentation,
+Algorithm 2 draws and prune/regrow results bit for bit.  Sizes span several
+segments and tiles with ragged tails; the full-size workloads are checked on
+sampled outputs (rows, columns, entries) that the oracle computes on their
+own."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity_util import (assert_close, canonical, check_products, check_topology, dev, sn,
+                         to_dev)
+
+pytestmark = pytest.mark.gpu
+
+ALL_B = [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 130]
+
+
+def _layer_case(out, inp, row, col, val, batches, seed=0, fused=True):
+    ref = canonical(out, inp, row, col, val)
+    h = sn().snack_create(out, inp, row, col, val)
+    check_topology(h, ref)
+    g = np.random.default_rng(seed)
+    for B in batches:
+        X = g.standard_normal((B, inp)).astype(np.float32)
+        dY = g.standard_normal((B, out)).astype(np.float32)
+        check_products(h, out, inp, ref, X, dY, fused=fused)
+    return h, ref
+
+
+# ------------------------------------------------------------ worked example
+
+def test_table7_example():
+    row, col, val = [2, 0, 1], [1, 2, 0], np.array([5, 3, 4], np.float32)
+    h, ref = _layer_case(3, 3, row, col, val, [1, 3, 8])
+    eye = to_dev(np.eye(3, dtype=np.float32))
+    Y = sn().snack_forward(h, eye).cpu().numpy()
+    assert np.array_equal(Y, np.array([[0, 4, 0], [0, 0, 5], [3, 0, 0]], np.float32))
+
+
+# ------------------------------------------------------------ workloads
+
+def test_toy256_all_batch_widths():
+    L = workloads.workload("toy256").layers[0]
+    row, col, val = L.coo()
+    _layer_case(L.out, L.inp, row, col, val, ALL_B, seed=1)
+
+
+@pytest.mark.parametrize("which", [0, 1])
+def test_gpt2_mlp_layers(which):
+    L = workloads.workload("gpt2_mlp").layers[which]
+    row, col, val = L.coo()
+    h, ref = _layer_case(L.out, L.inp, row, col, val, [], seed=2)
+    for B in (1, 8, 32):
+        X, dY = L.activations(B)
+        check_products(h, L.out, L.inp, ref, X, dY)
+
+
+def test_skewed_zipf_rows_full_size():
+    L = workloads.workload("skewed").layers[0]
+    row, col, val = L.coo()
+    h, ref = _layer_case(L.out, L.inp, row, col, val, [], seed=3)
+    # long rows are cut into several segments (split-row path)
+    _, _, segs = sn().snack_plan(h, 0, 16)
+    assert segs > L.out
+    for B in (1, 16):
+        X, dY = L.activations(B)
+        Y1, dX1, dW1 = check_products(h, L.out, L.inp, ref, X, dY)
+        # the split-row tickets re-arm: a second call gives identical bits
+        Y2 = sn().snack_forward(h, to_dev(X))
+        dX2 = sn().snack_backward_input(h, to_dev(dY))
+        torch.cuda.synchronize()
+        assert torch.equal(Y1, Y2) and torch.equal(dX1, dX2)
+
+
+def test_gpt2_decoder_block_layers_and_regrow():
+    wl = workloads.workload("gpt2_decoder")
+    for L in wl.layers[:4]:
+        row, col, val = L.coo()
+        h, ref = _layer_case(L.out, L.inp, row, col, val, [], seed=4)
+        X, dY = L.activations(256)
+        check_products(h, L.out, L.inp, ref, X, dY)
+        frac, seed = wl.extra["prune_frac"], 100 + L.seed
+        pruned, trials = sn().snack_prune_regrow(h, frac, seed)
+        o = oracle.prune_regrow(L.out, L.inp, ref["row"], ref["col"], ref["val"], frac, seed)
+        assert (pruned, trials) == (o["pruned"], o["trials"])
+        ref2 = canonical(L.out, L.inp, o["row"], o["col"], o["val"])
+        check_topology(h, ref2)
+        check_products(h, L.out, L.inp, ref2, X, dY, fused=False)
+
+
+def _sampled_large(sparsity, batches):
+    L = workloads.workload(f"large{sparsity}").layers[0]
+    row, col, val = L.coo()
+    ref = canonical(L.out, L.inp, row, col, val)
+    h = sn().snack_create(L.out, L.inp, row, col, val)
+    check_topology(h, ref)
+    g = np.random.default_rng(sparsity)
+    rows = np.sort(g.choice(L.out, 384, replace=False))
+    cols = np.sort(g.choice(L.inp, 384, replace=False))
+    ents = np.sort(g.choice(L.nnz, 4096, replace=False))
+    rp, cp = ref["row_ptr"], ref["col_ptr"]
+    rk = np.concatenate([np.arange(rp[r], rp[r + 1]) for r in rows])
+    ck = np.concatenate([ref["csc_perm"][cp[c]:cp[c + 1]] for c in cols])
+    m = sn()
+    for B in batches:
+        X, dY = L.activations(B)
+        Xd, dYd = to_dev(X), to_dev(dY)
+        Y = m.snack_forward(h, Xd)
+        dX, dW = m.snack_backward(h, Xd, dYd)
+        torch.cuda.synchronize()
+        Yo, Sy = oracle.forward(L.out, L.inp, ref["row"][rk], ref["col"][rk], ref["val"][rk], X)
+        assert_close(f"Y[{B}]", Y.cpu().numpy()[:, rows], Yo[:, rows], Sy[:, rows])
+        dXo, Sx = oracle.backward_input(L.out, L.inp, ref["row"][ck], ref["col"][ck],
+                                        ref["val"][ck], dY)
+        assert_close(f"dX[{B}]", dX.cpu().numpy()[:, cols], dXo[:, cols], Sx[:, cols])
+        dWo, Sw = oracle.backward_weight(L.out, L.inp, ref["row"][ents], ref["col"][ents], X, dY)
+        assert_close(f"dW[{B}]", dW.cpu().numpy()[ents], dWo, Sw)
+
+
+@pytest.mark.parametrize("sparsity", [99, 95, 90])
+def test_large_layer_full_size_sampled(sparsity):
+    _sampled_large(sparsity, [1, 4, 16, 64])
+
+
+def test_large99_full_oracle_b16():
+    # every output of the full-size 10000x10000 @99% layer at batch 16
+    L = workloads.workload("large99").layers[0]
+    row, col, val = L.coo()
+    h, ref = _layer_case(L.out, L.inp, row, col, val, [], seed=5)
+    X, dY = L.activations(16)
+    check_products(h, L.out, L.inp, ref, X, dY, fused=False)
+
+
+# ------------------------------------------------------------ edge cases
+
+def test_empty_layer_and_empty_lines():
+    m = sn()
+    h = m.snack_create(7, 5, np.zeros(0, np.int32), np.zeros(0, np.int32), np.zeros(0, np.float32))
+    X = to_dev(np.ones((3, 5), np.float32))
+    dY = to_dev(np.ones((3, 7), np.float32))
+    Y = m.snack_forward(h, X)
+    dX, dW = m.snack_backward(h, X, dY)
+    torch.cuda.synchronize()
+    assert torch.all(Y == 0) and torch.all(dX == 0) and dW.numel() == 0
+    # some empty rows and columns
+    row = np.array([0, 0, 4, 6], np.int32)
+    col = np.array([1, 4, 4, 0], np.int32)
+    val = np.array([1.5, -2.0, 3.0, 0.25], np.float32)
+    _layer_case(7, 5, row, col, val, [1, 4, 33])
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (1, 3000), (3000, 1), (16, 16), (64, 300)])
+def test_dense_patterns(shape):
+    out, inp = shape
+    row = np.repeat(np.arange(out), inp).astype(np.int32)
+    col = np.tile(np.arange(inp), out).astype(np.int32)
+    val = np.random.default_rng(6).standard_normal(out * inp).astype(np.float32)
+    _layer_case(out, inp, row, col, val, [1, 5, 16, 64])
+
+
+def test_long_rows_and_columns_split():
+    # three full rows of 20000 entries (rows split into many segments) and a
+    # matching skew in columns
+    g = np.random.default_rng(7)
+    out, inp = 40, 20000
+    cells = [np.arange(inp) + r * inp for r in (3, 17, 39)]
+    cells.append(g.choice(out * inp, 5000, replace=False))
+    cells = np.unique(np.concatenate(cells))
+    g.shuffle(cells)
+    row = (cells // inp).astype(np.int32)
+    col = (cells % inp).astype(np.int32)
+    val = g.standard_normal(cells.size).astype(np.float32)
+    h, _ = _layer_case(out, inp, row, col, val, [1, 8, 64, 70])
+    _, _, segs = sn().snack_plan(h, 0, 8)
+    assert segs > out
+
+
+def test_identity_pattern_bit_exact():
+    n = 4099
+    idx = np.arange(n, dtype=np.int32)
+    perm = np.random.default_rng(8).permutation(n)
+    h = sn().snack_create(n, n, idx[perm], idx[perm], np.ones(n, np.float32))
+    for B in (1, 3, 16, 64, 100):
+        X = to_dev(np.random.default_rng(B).standard_normal((B, n)).astype(np.float32))
+        Y = sn().snack_forward(h, X)
+        dX = sn().snack_backward_input(h, X)
+        torch.cuda.synchronize()
+        assert torch.equal(Y, X) and torch.equal(dX, X)
+
+
+def test_device_pointer_input_and_side_stream():
+    L = workloads.workload("toy256").layers[0]
+    row, col, val = L.coo()
+    ref = canonical(L.out, L.inp, row, col, val)
+    h = sn().snack_create(L.out, L.inp, to_dev(row), to_dev(col), to_dev(val))
+    check_topology(h, ref)
+    X, dY = L.activations(4)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        Y = sn().snack_forward(h, to_dev(X))
+    s.synchronize()
+    Yo, Sy = oracle.forward(L.out, L.inp, ref["row"], ref["col"], ref["val"], X)
+    assert_close("Y", Y, Yo, Sy)
+
+
+def test_values_view_updates_in_place():
+    L = workloads.workload("toy256").layers[0]
+    row, col, val = L.coo()
+    h = sn().snack_create(L.out, L.inp, row, col, val)
+    v = sn().snack_values(h)
+    ref = canonical(L.out, L.inp, row, col, val)
+    assert np.array_equal(v.cpu().numpy(), ref["val"])
+    v.mul_(2.0)
+    X, dY = L.activations(4)
+    check_products(h, L.out, L.inp, dict(ref, val=ref["val"] * 2), X, dY, fused=False)
+
+
+# ------------------------------------------------------------ errors
+
+def test_invalid_inputs_return_status():
+    m = sn()
+    with pytest.raises(m.SnackError) as e:
+        m.snack_create(4, 4, [0, 4], [0, 1], [1.0, 2.0])
+    assert e.value.status == 2
+    with pytest.raises(m.SnackError) as e:
+        m.snack_create(4, 4, [1, 2, 1], [3, 0, 3], [1.0, 2.0, 3.0])
+    assert e.value.status == 3
+    with pytest.raises(m.SnackError) as e:
+        m.snack_create(4, 4, [0, -1], [0, 1])
+    assert e.value.status == 2
+    h = m.snack_create(4, 4, [0, 1], [0, 1], [1.0, 2.0])
+    X = torch.zeros(3 * 4 + 1, device=dev())
+    with pytest.raises(m.SnackError) as e:      # misaligned X
+        m._check(m._lib.snack_forward(h.ptr, m._ptr(X[1:]), m._ptr(X[:12]), 3, m._stream(None)), h)
+    assert e.value.status == 1
+    with pytest.raises(m.SnackError) as e:      # batch 0
+        m._check(m._lib.snack_forward(h.ptr, m._ptr(X), m._ptr(X), 0, m._stream(None)), h)
+    assert e.value.status == 1
+    # the handle is still usable after rejected calls
+    Y = m.snack_forward(h, torch.ones(2, 4, device=dev()))
+    torch.cuda.synchronize()
+    assert Y.cpu().numpy().tolist() == [[1, 2, 0, 0], [1, 2, 0, 0]]
+
+
+# ------------------------------------------------------------ kernel choice
+
+def test_plan_follows_batch_and_row_length():
+    L = workloads.workload("large99").layers[0]
+    h, _ = sn().snack_create_random(L.out, L.inp, L.nnz, 1)
+    for B, w in ((1, 1), (2, 2), (3, 4), (5, 8), (16, 16), (17, 32), (64, 64), (300, 64)):
+        assert sn().snack_plan(h, 0, B)[0] == w
+    assert sn().snack_plan(h, 0, 16)[1] == 32            # 100 entries per row
+    small = workloads.workload("toy256").layers[0]
+    r, c, v = small.coo()
+    h2 = sn().snack_create(small.out, small.inp, r, c, v)
+    assert sn().snack_plan(h2, 0, 4)[1] == 4             # ~26 entries per row
+
+
+# ------------------------------------------------------------ Algorithm 2
+
+@pytest.mark.parametrize("shape", [(7, 9, 40), (300, 200, 6000), (3072, 768, 117965),
+                                   (1000, 1000, 990000)])
+def test_create_random_matches_oracle(shape):
+    out, inp, nnz = shape
+    for seed in (0, 12345):
+        h, trials = sn().snack_create_random(out, inp, nnz, seed)
+        r, c, _ = sn().snack_export(h)
+        orow, ocol, otrials = oracle.uniform_init(out, inp, nnz, seed)
+        assert trials == otrials
+        cells = np.sort(orow.astype(np.int64) * inp + ocol)
+        assert np.array_equal(r.astype(np.int64) * inp + c, cells)
+
+
+# ------------------------------------------------------------ prune / regrow
+
+@pytest.mark.parametrize("frac", [0.0, 0.05, 0.3, 1.0])
+def test_prune_regrow_matches_oracle(frac):
+    L = workloads.workload("gpt2_mlp").layers[0]
+    row, col, val = L.coo()
+    g = np.random.default_rng(9)
+    special = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-30, -1e-30], np.float32)
+    pick = g.choice(val.size, 500, replace=False)
+    val[pick] = special[g.integers(0, special.size, 500)]
+    val[g.choice(val.size, 2000, replace=False)] = 0.5  # many ties
+    ref = canonical(L.out, L.inp, row, col, val)
+    h = sn().snack_create(L.out, L.inp, row, col, val)
+    for step in range(3):
+        seed = 77 + step
+        p, t = sn().snack_prune_regrow(h, frac, seed)
+        o = oracle.prune_regrow(L.out, L.inp, ref["row"], ref["col"], ref["val"], frac, seed)
+        assert (p, t) == (o["pruned"], o["trials"])
+        ref = canonical(L.out, L.inp, o["row"], o["col"], o["val"])
+        check_topology(h, ref)
+
+
+def test_prune_regrow_dense_layer_reuses_pruned_cells():
+    out, inp = 8, 8
+    row = np.repeat(np.arange(out), inp).astype(np.int32)
+    col = np.tile(np.arange(inp), out).astype(np.int32)
+    val = np.arange(1, 65, dtype=np.float32)
+    ref = canonical(out, inp, row, col, val)
+    h = sn().snack_create(out, inp, row, col, val)
+    p, t = sn().snack_prune_regrow(h, 0.25, 5)
+    o = oracle.prune_regrow(out, inp, ref["row"], ref["col"], ref["val"], 0.25, 5)
+    assert (p, t) == (o["pruned"], o["trials"])
+    check_topology(h, canonical(out, inp, o["row"], o["col"], o["val"]))
+
+
+def test_prune_regrow_large_layer():
+    L = workloads.workload("large99").layers[0]
+    row, col, val = L.coo()
+    ref = canonical(L.out, L.inp, row, col, val)
+    h = sn().snack_create(L.out, L.inp, row, col, val)
+    p, t = sn().snack_prune_regrow(h, 0.3, 2024)
+    o = oracle.prune_regrow(L.out, L.inp, ref["row"], ref["col"], ref["val"], 0.3, 2024)
+    assert (p, t) == (o["pruned"], o["trials"])
+    assert p == math.floor(float(np.float32(0.3)) * L.nnz)
+    check_topology(h, canonical(L.out, L.inp, o["row"], o["col"], o["val"]))
