@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import glob
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -39,8 +40,17 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
+STAMP = os.path.join(BUILD, "machine.txt")
+
+
 def _stale() -> bool:
     if not os.path.exists(LIB):
+        return True
+    try:
+        with open(STAMP) as f:
+            if f.read().strip() != platform.machine():
+                return True  # built on another CPU architecture
+    except OSError:
         return True
     t = os.path.getmtime(LIB)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + \
@@ -76,6 +86,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(platform.machine())
     return LIB
 
 

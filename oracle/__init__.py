@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import threading
 
@@ -43,7 +44,13 @@ OK, ERR_RANGE, ERR_DUPLICATE, ERR_ALLOC, ERR_ARG = 0, 1, 2, 3, 4
 def build(force: bool = False) -> str:
     """Compile snack_oracle.c into oracle/_build/liboracle.so (plain gcc)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
-    if (not force and os.path.exists(_LIB_PATH)
+    stamp = os.path.join(_BUILD_DIR, "machine.txt")
+    try:
+        with open(stamp) as f:
+            same_machine = f.read().strip() == platform.machine()
+    except OSError:
+        same_machine = False
+    if (not force and same_machine and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
@@ -51,6 +58,8 @@ def build(force: bool = False) -> str:
                            "-fno-fast-math", "-ffp-contract=off",
                            _SRC, "-o", tmp, "-lm"])
     os.replace(tmp, _LIB_PATH)
+    with open(stamp, "w") as f:
+        f.write(platform.machine())
     return _LIB_PATH
 
 
