@@ -277,28 +277,39 @@ def run_ours(args):
     fl = flops_per_step(cases)
     value = world * fl * args.steps / (total_ms / 1e3) / 1e9
 
-    # Per-op durations (same stream, cold L2 each rep) -> dominant op, roofline.
+    # Per-op durations -> dominant op, roofline.  Each op is replayed from its
+    # own CUDA graph between events on the launching stream, after an L2
+    # flush that keeps the GPU busy while the host queues the replay.
     ops = []
     reps = max(5, min(50, args.steps))
+
+    def run_op(op, c, d):
+        if op == "fwd":
+            sn.snack_forward(c["h"], d["X"], d["Y"], stream=stream)
+        elif op == "bwd_input":
+            sn.snack_backward_input(c["h"], d["dY"], d["dX"], stream=stream)
+        else:
+            sn.snack_backward_weight(c["h"], d["X"], d["dY"], d["dW"], stream=stream)
+
     with torch.cuda.stream(stream):
         for c in cases:
             L = c["layer"]
             for B, d in c["dev"].items():
                 for op in ("fwd", "bwd_input", "bwd_weight"):
+                    g_op = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g_op, stream=stream):
+                        run_op(op, c, d)
+                    g_op.replay()
                     ts = []
                     for _ in range(reps):
                         flush.fill_(1.0)
                         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                         e0.record(stream)
-                        if op == "fwd":
-                            sn.snack_forward(c["h"], d["X"], d["Y"], stream=stream)
-                        elif op == "bwd_input":
-                            sn.snack_backward_input(c["h"], d["dY"], d["dX"], stream=stream)
-                        else:
-                            sn.snack_backward_weight(c["h"], d["X"], d["dY"], d["dW"], stream=stream)
+                        g_op.replay()
                         e1.record(stream)
                         ts.append((e0, e1))
                     torch.cuda.synchronize()
+                    del g_op
                     us = statistics.mean(a.elapsed_time(b) for a, b in ts) * 1e3
                     nbytes = metric_bytes(op, L.nnz, L.out, L.inp, B)
                     ops.append(dict(op=op, layer=L.name, shape=f"{L.out}x{L.inp}", nnz=L.nnz, B=B,

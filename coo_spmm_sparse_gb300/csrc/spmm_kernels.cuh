@@ -92,8 +92,68 @@ __device__ __forceinline__ void store_line(const SpmmArgs &a, int line, int sub,
     }
 }
 
+// Entries [kb, kb+4) of one group: indices / values from one 16-byte load
+// each, masked to the segment [k0, k1).
+template <bool PERM>
+__device__ __forceinline__ void load_quad(const SpmmArgs &a, int kb, int k0, int k1, int (&c)[4],
+                                          float (&w)[4]) {
+  const int4 c4 = ld_stream_i4(a.idx + kb);
+  c[0] = c4.x;
+  c[1] = c4.y;
+  c[2] = c4.z;
+  c[3] = c4.w;
+  if constexpr (PERM) {
+    const int4 p4 = ld_stream_i4(a.perm + kb);
+    const int pp[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = (kb + e >= k0 && kb + e < k1) ? __ldg(a.val + pp[e]) : 0.f;
+  } else {
+    const float4 v4 = ld_stream_f4(a.val + kb);
+    w[0] = v4.x;
+    w[1] = v4.y;
+    w[2] = v4.z;
+    w[3] = v4.w;
+  }
+}
+
+// Gather the lane's slice of the dense rows of up to 8 entries (all loads
+// issued before any use), then accumulate.
+template <int BW, int G, int Q>
+__device__ __forceinline__ void gather_fma(const float *src, const int (&c)[Q][4],
+                                           const float (&w)[Q][4], const bool (&ok)[Q][4],
+                                           float (&acc)[SliceShape<BW, G>::NV]
+                                                       [SliceShape<BW, G>::VEC]) {
+  using S = SliceShape<BW, G>;
+  constexpr int VEC = S::VEC, NV = S::NV;
+  float x[Q][4][NV][VEC];
+#pragma unroll
+  for (int q = 0; q < Q; ++q)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        if (ok[q][e]) {
+          load_vec<VEC>(src + (int64_t)c[q][e] * BW + v * G * VEC, x[q][e][v]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) x[q][e][v][i] = 0.f;
+        }
+      }
+#pragma unroll
+  for (int q = 0; q < Q; ++q)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) acc[v][i] = fmaf(w[q][e], x[q][e][v][i], acc[v][i]);
+}
+
 // One team of LPS lanes per segment; PERM = values reached through a
-// column-order -> canonical permutation (the dX = dY W direction).
+// column-order -> canonical permutation (the dX = dY W direction).  The grid
+// is persistent: teams stride over the segments in a warp-uniform loop so
+// that the warp-wide shuffles always see every lane.
 template <int BW, int G, int LPS, bool PERM>
 __global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
   using S = SliceShape<BW, G>;
@@ -103,149 +163,160 @@ __global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
   const int tlane = lane % LPS;
   const int grp = tlane / G;
   const int sub = tlane % G;
-  const int64_t team = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / LPS;
-  const bool active = team < a.nseg;
-  int4 sg = make_int4(0, 0, 0, -1);
-  if (active) sg = a.seg[team];
-  const int k0 = sg.y, k1 = sg.z;
-
-  float acc[NV][VEC];
-#pragma unroll
-  for (int v = 0; v < NV; ++v)
-#pragma unroll
-    for (int i = 0; i < VEC; ++i) acc[v][i] = 0.f;
-
+  const int64_t teams_per_block = blockDim.x / LPS;
+  const int64_t stride = (int64_t)gridDim.x * teams_per_block;
+  const int64_t my_team = (int64_t)blockIdx.x * teams_per_block + threadIdx.x / LPS;
+  const int64_t warp_team = (int64_t)blockIdx.x * teams_per_block + (threadIdx.x & ~31) / LPS;
   const float *src = a.src + sub * VEC;
-  for (int kb = (k0 & ~3) + 4 * grp; kb < k1; kb += 4 * NPT) {
-    const int4 c4 = ld_stream_i4(a.idx + kb);
-    float w[4];
-    if constexpr (PERM) {
-      const int4 p4 = ld_stream_i4(a.perm + kb);
-      const int pp[4] = {p4.x, p4.y, p4.z, p4.w};
+
+  for (int64_t t0 = 0; warp_team + t0 < a.nseg; t0 += stride) {
+    const int64_t team = my_team + t0;
+    const bool active = team < a.nseg;
+    int4 sg = make_int4(0, 0, 0, -1);
+    if (active) sg = a.seg[team];
+    const int k0 = sg.y, k1 = sg.z;
+
+    float acc[NV][VEC];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        w[e] = (kb + e >= k0 && kb + e < k1) ? __ldg(a.val + pp[e]) : 0.f;
-    } else {
-      const float4 v4 = ld_stream_f4(a.val + kb);
-      w[0] = v4.x;
-      w[1] = v4.y;
-      w[2] = v4.z;
-      w[3] = v4.w;
-    }
-    const int cc[4] = {c4.x, c4.y, c4.z, c4.w};
+    for (int v = 0; v < NV; ++v)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (kb + e >= k0 && kb + e < k1) {
-        const float *p = src + (int64_t)cc[e] * BW;
+      for (int i = 0; i < VEC; ++i) acc[v][i] = 0.f;
+
+    int kb = (k0 & ~3) + 4 * grp;
+    for (; kb + 4 * NPT < k1; kb += 8 * NPT) {  // two quads in flight
+      int c[2][4];
+      float w[2][4];
+      bool ok[2][4];
+      load_quad<PERM>(a, kb, k0, k1, c[0], w[0]);
+      load_quad<PERM>(a, kb + 4 * NPT, k0, k1, c[1], w[1]);
 #pragma unroll
-        for (int v = 0; v < NV; ++v) {
-          float x[VEC];
-          load_vec<VEC>(p + v * G * VEC, x);
+      for (int q = 0; q < 2; ++q)
 #pragma unroll
-          for (int i = 0; i < VEC; ++i) acc[v][i] = fmaf(w[e], x[i], acc[v][i]);
+        for (int e = 0; e < 4; ++e) {
+          const int k = kb + q * 4 * NPT + e;
+          ok[q][e] = k >= k0 && k < k1;
         }
-      }
+      gather_fma<BW, G, 2>(src, c, w, ok, acc);
     }
-  }
+    if (kb < k1) {
+      int c[1][4];
+      float w[1][4];
+      bool ok[1][4];
+      load_quad<PERM>(a, kb, k0, k1, c[0], w[0]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ok[0][e] = kb + e >= k0 && kb + e < k1;
+      gather_fma<BW, G, 1>(src, c, w, ok, acc);
+    }
 
-  // Combine the NPT groups of the team (every lane of the warp gets here).
+    // Combine the NPT groups of the team (every lane of the warp is here).
 #pragma unroll
-  for (int off = G; off < LPS; off <<= 1)
-#pragma unroll
-    for (int v = 0; v < NV; ++v)
-#pragma unroll
-      for (int i = 0; i < VEC; ++i) acc[v][i] += __shfl_xor_sync(0xffffffffu, acc[v][i], off);
-
-  if (!active) return;
-  const int line = sg.x;
-  if (sg.w < 0) {
-    if (grp == 0) store_line<BW, G>(a, line, sub, acc);
-    return;
-  }
-
-  // Line split over several segments: park the partial, last arrival sums.
-  const int4 sp = a.split[sg.w];  // {first segment, parts, first slot, 0}
-  const int part = (int)(team - sp.x);
-  if (grp == 0) {
-    float *mine = a.partial + (int64_t)(sp.z + part) * BW + sub * VEC;
-#pragma unroll
-    for (int v = 0; v < NV; ++v)
-#pragma unroll
-      for (int i = 0; i < VEC; ++i) mine[v * G * VEC + i] = acc[v][i];
-  }
-  __threadfence();
-  const unsigned tmask = LPS == 32 ? 0xffffffffu : (((1u << LPS) - 1u) << (lane - tlane));
-  __syncwarp(tmask);
-  int last = 0;
-  if (tlane == 0) last = atomicAdd(a.counter + sg.w, 1) == sp.y - 1;
-  last = __shfl_sync(tmask, last, lane - tlane);
-  if (!last) return;
-  __threadfence();
-  if (grp == 0) {
-    float tot[NV][VEC];
-#pragma unroll
-    for (int v = 0; v < NV; ++v)
-#pragma unroll
-      for (int i = 0; i < VEC; ++i) tot[v][i] = 0.f;
-    for (int p = 0; p < sp.y; ++p) {
-      const float *q = a.partial + (int64_t)(sp.z + p) * BW + sub * VEC;
+    for (int off = G; off < LPS; off <<= 1)
 #pragma unroll
       for (int v = 0; v < NV; ++v)
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) tot[v][i] += __ldcg(q + v * G * VEC + i);
+        for (int i = 0; i < VEC; ++i) acc[v][i] += __shfl_xor_sync(0xffffffffu, acc[v][i], off);
+
+    if (!active) continue;
+    const int line = sg.x;
+    if (sg.w < 0) {
+      if (grp == 0) store_line<BW, G>(a, line, sub, acc);
+      continue;
     }
-    store_line<BW, G>(a, line, sub, tot);
+
+    // Line split over several segments: park the partial, last arrival sums.
+    const int4 sp = a.split[sg.w];  // {first segment, parts, first slot, 0}
+    const int part = (int)(team - sp.x);
+    if (grp == 0) {
+      float *mine = a.partial + (int64_t)(sp.z + part) * BW + sub * VEC;
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) mine[v * G * VEC + i] = acc[v][i];
+    }
+    __threadfence();
+    const unsigned tmask = LPS == 32 ? 0xffffffffu : (((1u << LPS) - 1u) << (lane - tlane));
+    __syncwarp(tmask);
+    int last = 0;
+    if (tlane == 0) last = atomicAdd(a.counter + sg.w, 1) == sp.y - 1;
+    last = __shfl_sync(tmask, last, lane - tlane);
+    if (!last) continue;
+    __threadfence();
+    if (grp == 0) {
+      float tot[NV][VEC];
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) tot[v][i] = 0.f;
+      for (int p = 0; p < sp.y; ++p) {
+        const float *q = a.partial + (int64_t)(sp.z + p) * BW + sub * VEC;
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) tot[v][i] += __ldcg(q + v * G * VEC + i);
+      }
+      store_line<BW, G>(a, line, sub, tot);
+    }
+    if (tlane == 0) a.counter[sg.w] = 0;  // re-arm for the next call
   }
-  if (tlane == 0) a.counter[sg.w] = 0;  // re-arm for the next call
 }
 
 // dW[k] = sum_b dY[b][row_k] X[b][col_k] over the row segments; the G lanes
 // of a group each form part of the batch dot product and meet by shuffle.
-template <int BW, int G, int LPS>
-__global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
+// Persistent grid; a team's lanes stay together, groups never diverge.
+template <int BW, int G>
+__device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt, int kb, int k0,
+                                            int k1, int npt, unsigned gmask, int sub,
+                                            const float (&dy)[SliceShape<BW, G>::NV]
+                                                             [SliceShape<BW, G>::VEC],
+                                            bool two) {
   using S = SliceShape<BW, G>;
-  constexpr int VEC = S::VEC, NV = S::NV, NPT = LPS / G;
-  const int lane = threadIdx.x & 31;
-  const int tlane = lane % LPS;
-  const int grp = tlane / G;
-  const int sub = tlane % G;
-  const int64_t team = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / LPS;
-  if (team >= a.nseg) return;  // whole teams (and so whole groups) leave together
-  const unsigned gmask = G == 1 ? (1u << lane) : (((1u << G) - 1u) << (lane & ~(G - 1)));
-  const int4 sg = a.seg[team];
-  const int r = sg.x, k0 = sg.y, k1 = sg.z;
-
-  float dy[NV][VEC];
-  {
-    const float *p = a.dyt + (int64_t)r * BW + sub * VEC;
+  constexpr int VEC = S::VEC, NV = S::NV;
+  int c[2][4];
+  float x[2][4][NV][VEC];
 #pragma unroll
-    for (int v = 0; v < NV; ++v) load_vec<VEC>(p + v * G * VEC, dy[v]);
+  for (int q = 0; q < 2; ++q) {
+    if (q == 1 && !two) break;
+    const int4 c4 = ld_stream_i4(a.col + kb + q * 4 * npt);
+    c[q][0] = c4.x;
+    c[q][1] = c4.y;
+    c[q][2] = c4.z;
+    c[q][3] = c4.w;
   }
-  const float *xt = a.xt + sub * VEC;
-  for (int kb = (k0 & ~3) + 4 * grp; kb < k1; kb += 4 * NPT) {
-    const int4 c4 = ld_stream_i4(a.col + kb);
-    const int cc[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int k = kb + q * 4 * npt + e;
+      const bool ok = (q == 0 || two) && k >= k0 && k < k1;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        if (ok) {
+          load_vec<VEC>(xt + (int64_t)c[q][e] * BW + v * G * VEC, x[q][e][v]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) x[q][e][v][i] = 0.f;
+        }
+      }
+    }
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    if (q == 1 && !two) break;
+    const int kq = kb + q * 4 * npt;
     float res[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       float s = 0.f;
-      if (kb + e >= k0 && kb + e < k1) {
-        const float *p = xt + (int64_t)cc[e] * BW;
 #pragma unroll
-        for (int v = 0; v < NV; ++v) {
-          float x[VEC];
-          load_vec<VEC>(p + v * G * VEC, x);
+      for (int v = 0; v < NV; ++v)
 #pragma unroll
-          for (int i = 0; i < VEC; ++i) s = fmaf(dy[v][i], x[i], s);
-        }
-      }
+        for (int i = 0; i < VEC; ++i) s = fmaf(dy[v][i], x[q][e][v][i], s);
 #pragma unroll
       for (int off = 1; off < G; off <<= 1) s += __shfl_xor_sync(gmask, s, off);
       res[e] = s;
     }
     if (sub == 0) {
-      float *d = a.dw + kb;
-      if (kb >= k0 && kb + 3 < k1) {
+      float *d = a.dw + kq;
+      if (kq >= k0 && kq + 3 < k1) {
         float4 o = make_float4(res[0], res[1], res[2], res[3]);
         if (a.accumulate) {
           const float4 old = *reinterpret_cast<const float4 *>(d);
@@ -258,9 +329,38 @@ __global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (kb + e >= k0 && kb + e < k1) d[e] = a.accumulate ? d[e] + res[e] : res[e];
+          if (kq + e >= k0 && kq + e < k1) d[e] = a.accumulate ? d[e] + res[e] : res[e];
       }
     }
+  }
+}
+
+template <int BW, int G, int LPS>
+__global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
+  using S = SliceShape<BW, G>;
+  constexpr int VEC = S::VEC, NV = S::NV, NPT = LPS / G;
+  const int lane = threadIdx.x & 31;
+  const int tlane = lane % LPS;
+  const int grp = tlane / G;
+  const int sub = tlane % G;
+  const unsigned gmask = G == 1 ? (1u << lane) : (((1u << G) - 1u) << (lane & ~(G - 1)));
+  const int64_t teams_per_block = blockDim.x / LPS;
+  const int64_t stride = (int64_t)gridDim.x * teams_per_block;
+  const float *xt = a.xt + sub * VEC;
+  for (int64_t team = (int64_t)blockIdx.x * teams_per_block + threadIdx.x / LPS; team < a.nseg;
+       team += stride) {
+    const int4 sg = a.seg[team];
+    const int r = sg.x, k0 = sg.y, k1 = sg.z;
+    float dy[NV][VEC];
+    {
+      const float *p = a.dyt + (int64_t)r * BW + sub * VEC;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) load_vec<VEC>(p + v * G * VEC, dy[v]);
+    }
+    int kb = (k0 & ~3) + 4 * grp;
+    for (; kb + 4 * NPT < k1; kb += 8 * NPT)
+      sddmm_quads<BW, G>(a, xt, kb, k0, k1, NPT, gmask, sub, dy, true);
+    if (kb < k1) sddmm_quads<BW, G>(a, xt, kb, k0, k1, NPT, gmask, sub, dy, false);
   }
 }
 

@@ -50,7 +50,8 @@ def check_topology(h, ref):
     r, c, v = m.snack_export(h)
     assert np.array_equal(r, ref["row"])
     assert np.array_equal(c, ref["col"])
-    assert np.array_equal(v, ref["val"])
+    # values compared bit for bit (NaN payloads and signed zeros included)
+    assert np.array_equal(v.view(np.uint32), np.asarray(ref["val"], np.float32).view(np.uint32))
     seg = m.snack_export_segments(h)
     for k in ("row_ptr", "col_ptr", "csc_row", "csc_perm"):
         assert np.array_equal(seg[k], ref[k]), k
