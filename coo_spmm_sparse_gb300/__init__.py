@@ -33,7 +33,7 @@ __all__ = [
     "SnackError", "SnackHandle", "snack_create", "snack_create_random", "snack_forward",
     "snack_backward_input", "snack_backward_weight", "snack_backward", "snack_prune_regrow",
     "snack_values", "snack_export", "snack_export_segments", "snack_plan", "snack_nnz",
-    "snack_device_bytes", "snack_destroy", "snack_launch_count", "SnackLinear", "library_path",
+    "snack_device_bytes", "snack_destroy", "snack_launch_count", "snack_forward_csr_static", "SnackLinear", "library_path",
 ]
 
 
@@ -254,6 +254,28 @@ def snack_plan(h: SnackHandle, op: int, batch: int):
     w, l, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
     _check(_lib.snack_plan(h.ptr, op, batch, ctypes.byref(w), ctypes.byref(l), ctypes.byref(s)), h)
     return int(w.value), int(l.value), int(s.value)
+
+
+def snack_forward_csr_static(out: int, inp: int, row_ptr: torch.Tensor, col: torch.Tensor,
+                             val: torch.Tensor, X: torch.Tensor, Y: torch.Tensor | None = None,
+                             stream=None) -> torch.Tensor:
+    """Y = X W^T from caller-held CSR arrays, with the library's fixed device
+    scratch instead of any allocation (for callers that cannot allocate when
+    they run the layer).  Allocates Y only if it is not given."""
+    X = _dev_f32(X, "X")
+    B = _batch(X, inp, "X")
+    for t, name, dt in ((row_ptr, "row_ptr", torch.int32), (col, "col", torch.int32),
+                        (val, "val", torch.float32)):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == dt and t.is_contiguous()):
+            raise TypeError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if Y is None:
+        Y = torch.empty((B, out), dtype=torch.float32, device=X.device)
+    _dev_f32(Y, "Y")
+    nnz = int(col.numel())
+    _check(_lib.snack_forward_csr_static(out, inp, nnz, _ptr(row_ptr), _ptr(col) if nnz else None,
+                                         _ptr(val) if nnz else None, _ptr(X), _ptr(Y), B,
+                                         _stream(stream, X.device)))
+    return Y
 
 
 def snack_launch_count() -> int:

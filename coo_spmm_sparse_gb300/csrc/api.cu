@@ -162,6 +162,12 @@ snack_status run_sddmm_slice(snack_handle h, const float *X, const float *dY, fl
 
 }  // namespace
 
+namespace snack {
+// Failures of entry points that have no handle report through
+// snack_last_error(NULL), like snack_create.
+void record_thread_error(const std::string &msg) { g_create_error = msg; }
+}  // namespace snack
+
 extern "C" {
 
 snack_status snack_create(int64_t out_features, int64_t in_features, int64_t nnz,

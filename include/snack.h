@@ -181,6 +181,40 @@ snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_wi
                         int32_t *lanes_per_segment, int64_t *segments);
 
 /*
+ * Forward pass Y = X W^T for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that hold no allocation rights when they run the layer: code that runs
+ * while a CUDA graph is captured in global mode (cudaMalloc is not allowed
+ * there), serving loops whose device memory is already reserved by another
+ * allocator, and latency-critical paths where an allocation's implicit
+ * device synchronisation is not acceptable.  It needs no handle and
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *
+ *   row_ptr [out_features+1], col [nnz], val [nnz]: a CSR layout of W in the
+ *     caller's device memory, e.g. as exported by snack_export_segments()
+ *     and snack_export().  Not validated: row_ptr must be non-decreasing
+ *     with row_ptr[0] = 0 and row_ptr[out_features] = nnz, and every col
+ *     must lie in [0, in_features).  col and val must be 16-byte aligned.
+ *   X [batch][in_features] in, Y [batch][out_features] out (overwritten),
+ *     16-byte aligned device memory, as for snack_forward().
+ * Its only scratch is a fixed 8 MiB array (2^21 floats) in the library's
+ * device memory, which every GPU that loads the library holds until the
+ * process exits.  It holds the transposed X slice, so in_features times the
+ * batch slice width (batch rounded up to a power of two, at most 64; no
+ * scratch for batch 1) must not exceed 2^21, else SNACK_ERR_UNSUPPORTED.
+ * The scratch is rewritten in full by every call.  All calls share it:
+ * calls whose work overlaps on the GPU (other streams, other threads) race.
+ * The first call on a device looks up the scratch's device address; make
+ * that first call before any stream capture.  Rows are not split, so a few
+ * very long rows run slower than with snack_forward().  Errors are reported
+ * through snack_last_error(NULL).  Asynchronous on `stream`.
+ */
+snack_status snack_forward_csr_static(int64_t out_features, int64_t in_features, int64_t nnz,
+                                      const int32_t *row_ptr, const int32_t *col,
+                                      const float *val, const float *X, float *Y,
+                                      int64_t batch, void *stream);
+
+/*
  * Kernel launches this library has issued in the process so far (all
  * handles, all threads).  Launches recorded into a CUDA graph count once,
  * at capture.  For accounting and tests.
