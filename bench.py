@@ -475,6 +475,34 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_only_op(args):
+    """One op, a few launches, for an ncu capture of a single kernel."""
+    import torch
+    import coo_spmm_sparse_gb300 as sn
+    wl, cases = make_cases(args.workload, args.batches, args.seed)
+    c = cases[0]
+    L = c["layer"]
+    B = sorted(c["acts"])[0]
+    X, dY = (torch.from_numpy(a).cuda() for a in c["acts"][B])
+    h = sn.snack_create(L.out, L.inp, c["row"], c["col"], c["val"])
+    Y = torch.empty(B, L.out, device="cuda")
+    dX = torch.empty(B, L.inp, device="cuda")
+    dW = torch.empty(L.nnz, device="cuda")
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda")
+    for _ in range(args.reps):
+        flush.fill_(1.0)
+        if args.only_op == "fwd":
+            sn.snack_forward(h, X, Y)
+        elif args.only_op == "bwd_input":
+            sn.snack_backward_input(h, dY, dX)
+        elif args.only_op == "bwd_weight":
+            sn.snack_backward_weight(h, X, dY, dW)
+        else:
+            sn.snack_backward(h, X, dY, dX, dW)
+    torch.cuda.synchronize()
+    print(f"only-op {args.only_op} {L.name} {L.out}x{L.inp} nnz={L.nnz} B={B} reps={args.reps}")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -487,9 +515,16 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-op", choices=["fwd", "bwd_input", "bwd_weight", "bwd"], default=None,
+                    help="profiling mode: run one op --reps times on the first layer and "
+                         "batch of the workload (cold L2 before each), print no JSON")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.only_op:
+        run_only_op(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -87,76 +87,91 @@ snack_status finish_create(snack_layer *h, snack_status st, const std::string &e
   return SNACK_OK;
 }
 
-// Run the segmented SpMM over batch slices of at most 64.
-//   rows == true : Y  = X W^T   (row segments, src = X,  lines = out)
-//   rows == false: dX = dY W    (column segments, src = dY, lines = in)
-snack_status run_spmm(snack_handle h, bool rows, const float *src, float *dst, int64_t batch,
-                      cudaStream_t s) {
-  snack::Layer &L = h->L;
+snack::SpmmArgs spmm_args(snack::Layer &L, bool rows, const float *op, float *dst, int nb) {
   const snack::SegTable &tab = rows ? L.csr : L.csc;
-  const int64_t src_lines = rows ? L.in : L.out;  // width of the dense operand
-  const int64_t dst_lines = rows ? L.out : L.in;
-  float *ws = rows ? L.d_xt : L.d_dyt;
+  snack::SpmmArgs a;
+  a.seg = tab.d_seg;
+  a.nseg = tab.nseg;
+  a.split = tab.d_split;
+  a.idx = rows ? L.d_col : L.d_csc_row;
+  a.val = L.d_val;
+  a.perm = rows ? nullptr : L.d_csc_perm;
+  a.src = op;
+  a.dst = dst;
+  a.ld = rows ? L.out : L.in;
+  a.nb = nb;
+  a.partial = L.d_partial;
+  a.counter = L.d_counter;
+  a.lps = 32;
+  return a;
+}
+
+// Forward Y = X W^T over batch slices of at most 64: the slice of X is
+// transposed into the workspace (not needed for a single row), then the
+// row-segment kernel runs as a programmatic dependent of that transpose.
+snack_status run_forward(snack_handle h, const float *X, float *Y, int64_t batch, cudaStream_t s) {
+  snack::Layer &L = h->L;
   for (int64_t b0 = 0; b0 < batch; b0 += snack::kMaxSlice) {
     const int nb = (int)std::min<int64_t>(snack::kMaxSlice, batch - b0);
-    const snack::Plan p = snack::choose_plan(tab, nb);
-    const float *op = src + b0 * src_lines;
-    if (p.bw > 1) {
-      cudaError_t e = snack::launch_transpose(op, src_lines, nb, src_lines, ws, p.bw, s);
+    const snack::Plan p = snack::choose_plan(L.csr, nb);
+    const float *op = X + b0 * L.in;
+    const bool transposed = p.bw > 1;
+    if (transposed) {
+      cudaError_t e = snack::launch_transpose(op, L.in, nb, L.in, L.d_xt, p.bw, s);
       if (e != cudaSuccess) return cuda_fail(h, e, "transpose launch");
       g_launches.fetch_add(1, std::memory_order_relaxed);
-      op = ws;
+      op = L.d_xt;
     }
-    snack::SpmmArgs a;
-    a.seg = tab.d_seg;
-    a.nseg = tab.nseg;
-    a.split = tab.d_split;
-    a.idx = rows ? L.d_col : L.d_csc_row;
-    a.val = L.d_val;
-    a.perm = rows ? nullptr : L.d_csc_perm;
-    a.src = op;
-    a.dst = dst + b0 * dst_lines;
-    a.ld = dst_lines;
-    a.nb = nb;
-    a.partial = L.d_partial;
-    a.counter = L.d_counter;
-    cudaError_t e = rows ? snack::launch_spmm_rows(p, a, s) : snack::launch_spmm_cols(p, a, s);
-    if (e != cudaSuccess) return cuda_fail(h, e, "spmm launch");
-    if (a.nseg > 0) g_launches.fetch_add(1, std::memory_order_relaxed);
+    const snack::SpmmArgs a = spmm_args(L, true, op, Y + b0 * L.out, nb);
+    cudaError_t e = snack::launch_spmm_rows(p, a, transposed, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "forward launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
   }
   return SNACK_OK;
 }
 
-// dW over batch slices; dyt_ready: slice's dY^T already in the workspace.
-snack_status run_sddmm_slice(snack_handle h, const float *X, const float *dY, float *dW,
-                             int64_t b0, int nb, bool dyt_ready, cudaStream_t s) {
+// One batch slice of the backward: dX (if dX) and / or dW (if dW).  One
+// launch transposes the slices of dY (and X when dW is wanted); one launch
+// then computes what is asked, both products sharing the transposed dY.
+snack_status run_backward_slice(snack_handle h, const float *X, const float *dY, float *dX,
+                                float *dW, int64_t b0, int nb, cudaStream_t s) {
   snack::Layer &L = h->L;
-  const snack::Plan p = snack::choose_plan(L.csr, nb);
-  const float *xt = X + b0 * L.in;
+  const snack::Plan pc = snack::choose_plan(L.csc, nb);
+  const snack::Plan pr = snack::choose_plan(L.csr, nb);
+  const float *xt = dW ? X + b0 * L.in : nullptr;
   const float *dyt = dY + b0 * L.out;
-  if (p.bw > 1) {
-    cudaError_t e = snack::launch_transpose(xt, L.in, nb, L.in, L.d_xt, p.bw, s);
+  const bool transposed = pc.bw > 1;
+  if (transposed) {
+    cudaError_t e = dW ? snack::launch_transpose_pair(dyt, L.out, L.out, L.d_dyt, xt, L.in, L.in,
+                                                      L.d_xt, nb, pc.bw, s)
+                       : snack::launch_transpose(dyt, L.out, nb, L.out, L.d_dyt, pc.bw, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "transpose launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    xt = L.d_xt;
-    if (!dyt_ready) {
-      e = snack::launch_transpose(dyt, L.out, nb, L.out, L.d_dyt, p.bw, s);
-      if (e != cudaSuccess) return cuda_fail(h, e, "transpose launch");
-      g_launches.fetch_add(1, std::memory_order_relaxed);
-    }
     dyt = L.d_dyt;
+    if (dW) xt = L.d_xt;
   }
-  snack::SddmmArgs a;
-  a.seg = L.csr.d_seg;
-  a.nseg = L.csr.nseg;
-  a.col = L.d_col;
-  a.xt = xt;
-  a.dyt = dyt;
-  a.dw = dW;
-  a.accumulate = b0 > 0;
-  cudaError_t e = snack::launch_sddmm(p, a, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "sddmm launch");
-  if (a.nseg > 0) g_launches.fetch_add(1, std::memory_order_relaxed);
+  snack::SpmmArgs cols;
+  if (dX) cols = spmm_args(L, false, dyt, dX + b0 * L.in, nb);
+  snack::SddmmArgs rows;
+  if (dW) {
+    rows.seg = L.csr.d_seg;
+    rows.nseg = L.csr.nseg;
+    rows.col = L.d_col;
+    rows.xt = xt;
+    rows.dyt = dyt;
+    rows.dw = dW;
+    rows.accumulate = b0 > 0;
+    rows.lps = 32;
+  }
+  cudaError_t e;
+  if (dX && dW)
+    e = snack::launch_backward_fused(pc, cols, pr, rows, transposed, s);
+  else if (dX)
+    e = snack::launch_spmm_cols(pc, cols, transposed, s);
+  else
+    e = snack::launch_sddmm(pr, rows, transposed, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "backward launch");
+  g_launches.fetch_add(1, std::memory_order_relaxed);
   return SNACK_OK;
 }
 
@@ -259,7 +274,7 @@ snack_status snack_forward(snack_handle h, const float *X, float *Y, int64_t bat
   if ((st = check_dense(h, X, "X")) != SNACK_OK || (st = check_dense(h, Y, "Y")) != SNACK_OK ||
       (st = check_device(h)) != SNACK_OK)
     return st;
-  return run_spmm(h, true, X, Y, batch, static_cast<cudaStream_t>(stream));
+  return run_forward(h, X, Y, batch, static_cast<cudaStream_t>(stream));
 }
 
 snack_status snack_backward_input(snack_handle h, const float *dY, float *dX, int64_t batch,
@@ -270,7 +285,12 @@ snack_status snack_backward_input(snack_handle h, const float *dY, float *dX, in
   if ((st = check_dense(h, dY, "dY")) != SNACK_OK || (st = check_dense(h, dX, "dX")) != SNACK_OK ||
       (st = check_device(h)) != SNACK_OK)
     return st;
-  return run_spmm(h, false, dY, dX, batch, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int64_t b0 = 0; b0 < batch; b0 += snack::kMaxSlice) {
+    const int nb = (int)std::min<int64_t>(snack::kMaxSlice, batch - b0);
+    if ((st = run_backward_slice(h, nullptr, dY, dX, nullptr, b0, nb, s)) != SNACK_OK) return st;
+  }
+  return SNACK_OK;
 }
 
 snack_status snack_backward_weight(snack_handle h, const float *X, const float *dY, float *dW,
@@ -284,7 +304,7 @@ snack_status snack_backward_weight(snack_handle h, const float *X, const float *
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (int64_t b0 = 0; b0 < batch; b0 += snack::kMaxSlice) {
     const int nb = (int)std::min<int64_t>(snack::kMaxSlice, batch - b0);
-    if ((st = run_sddmm_slice(h, X, dY, dW, b0, nb, false, s)) != SNACK_OK) return st;
+    if ((st = run_backward_slice(h, X, dY, nullptr, dW, b0, nb, s)) != SNACK_OK) return st;
   }
   return SNACK_OK;
 }
@@ -303,10 +323,7 @@ snack_status snack_backward(snack_handle h, const float *X, const float *dY, flo
   snack::Layer &L = h->L;
   for (int64_t b0 = 0; b0 < batch; b0 += snack::kMaxSlice) {
     const int nb = (int)std::min<int64_t>(snack::kMaxSlice, batch - b0);
-    // One dY^T per slice serves both products when their slice widths agree
-    // (they do: the width depends on the batch slice only).
-    if (dX && (st = run_spmm(h, false, dY + b0 * L.out, dX + b0 * L.in, nb, s)) != SNACK_OK) return st;
-    if (dW && (st = run_sddmm_slice(h, X, dY, dW, b0, nb, dX != nullptr, s)) != SNACK_OK) return st;
+    if ((st = run_backward_slice(h, X, dY, dX, dW, b0, nb, s)) != SNACK_OK) return st;
   }
   return SNACK_OK;
 }

@@ -1,26 +1,40 @@
-// Backward-weight SDDMM, the dense-operand transpose, and kernel selection.
+// Backward-weight SDDMM, the dense-operand transposes, and kernel selection.
 #include "spmm_dispatch.cuh"
 
 namespace snack {
 
-cudaError_t launch_sddmm(const Plan &p, const SddmmArgs &a, cudaStream_t s) {
-  SNACK_WIDTH_CASES(sddmm_segments, )
+cudaError_t launch_sddmm(const Plan &p, const SddmmArgs &args, bool pdl, cudaStream_t s) {
+  if (args.nseg == 0) return cudaSuccess;
+  SddmmArgs a = args;
+  a.lps = team_lanes(p);
+  const int64_t need = (a.nseg * a.lps + 255) / 256;
+#define SNACK_CALL(W, L)                                        \
+  {                                                             \
+    auto k = sddmm_segments<W, L>;                              \
+    const int64_t cap = resident_capacity(k);                   \
+    return launch_ex(k, need < cap ? need : cap, pdl, s, a);    \
+  }
+  SNACK_BW_LPS_SWITCH(p.bw, a.lps, SNACK_CALL)
+#undef SNACK_CALL
 }
 
 cudaError_t launch_transpose(const float *src, int64_t ld, int nb, int64_t ncols, float *dst,
                              int bw, cudaStream_t s) {
-  if (ncols == 0) return cudaSuccess;
-  const int64_t grid = (ncols + 31) / 32;
-  switch (bw) {
-    case 2: transpose_pad<2><<<(unsigned)grid, 256, 0, s>>>(src, ld, nb, ncols, dst); break;
-    case 4: transpose_pad<4><<<(unsigned)grid, 256, 0, s>>>(src, ld, nb, ncols, dst); break;
-    case 8: transpose_pad<8><<<(unsigned)grid, 256, 0, s>>>(src, ld, nb, ncols, dst); break;
-    case 16: transpose_pad<16><<<(unsigned)grid, 256, 0, s>>>(src, ld, nb, ncols, dst); break;
-    case 32: transpose_pad<32><<<(unsigned)grid, 256, 0, s>>>(src, ld, nb, ncols, dst); break;
-    case 64: transpose_pad<64><<<(unsigned)grid, 256, 0, s>>>(src, ld, nb, ncols, dst); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  const int64_t tiles = (ncols + 31) / 32;
+#define SNACK_CALL(W) return launch_ex(transpose_pad<W>, tiles, false, s, src, ld, nb, ncols, dst);
+  SNACK_BW_SWITCH(bw, SNACK_CALL)
+#undef SNACK_CALL
+}
+
+cudaError_t launch_transpose_pair(const float *a, int64_t a_ld, int64_t a_cols, float *at,
+                                  const float *b, int64_t b_ld, int64_t b_cols, float *bt, int nb,
+                                  int bw, cudaStream_t s) {
+  const int64_t a_tiles = (a_cols + 31) / 32, b_tiles = (b_cols + 31) / 32;
+#define SNACK_CALL(W)                                                                      \
+  return launch_ex(transpose_pair<W>, a_tiles + b_tiles, false, s, a, a_ld, a_cols, at, b, \
+                   b_ld, b_cols, bt, nb, a_tiles);
+  SNACK_BW_SWITCH(bw, SNACK_CALL)
+#undef SNACK_CALL
 }
 
 int slice_width(int64_t nb) {
@@ -32,7 +46,7 @@ int slice_width(int64_t nb) {
 int entry_lanes(int bw) { return lanes_for(bw); }
 
 // Team size: a group takes 4 entries per step; aim for about two steps per
-// group on an average segment, between 4 and 32 lanes.
+// group on an average segment, between 8 and 32 lanes.
 Plan choose_plan(const SegTable &t, int64_t nb) {
   Plan p;
   p.bw = slice_width(nb < kMaxSlice ? nb : kMaxSlice);
@@ -41,7 +55,7 @@ Plan choose_plan(const SegTable &t, int64_t nb) {
   int npt = 1;
   while (npt < want && npt * g < 32) npt <<= 1;
   int lanes = npt * g;
-  if (lanes < 4) lanes = 4;
+  if (lanes < 8) lanes = 8;
   if (lanes > 32) lanes = 32;
   p.lanes = lanes;
   return p;

@@ -76,6 +76,7 @@ struct SpmmArgs {
   int nb;               // valid batch rows in this slice
   float *partial;
   int *counter;
+  int lps;              // lanes per segment team (set by the launcher)
 };
 
 struct SddmmArgs {
@@ -86,6 +87,7 @@ struct SddmmArgs {
   const float *dyt;  // [out][bw]
   float *dw;         // [nnz]
   int accumulate;    // add to dw instead of overwriting (batch slices > 0)
+  int lps;           // lanes per segment team (set by the launcher)
 };
 
 // Kernel selection: batch slice width, lanes per entry group, lanes per segment.
@@ -98,9 +100,17 @@ Plan choose_plan(const SegTable &t, int64_t nb);
 int entry_lanes(int bw);
 
 // Launchers (spmm_*.cu).  Return the launch's cudaError_t.
-cudaError_t launch_spmm_rows(const Plan &p, const SpmmArgs &a, cudaStream_t s);
-cudaError_t launch_spmm_cols(const Plan &p, const SpmmArgs &a, cudaStream_t s);
-cudaError_t launch_sddmm(const Plan &p, const SddmmArgs &a, cudaStream_t s);
+// pdl: launch as a programmatic dependent of the previous kernel on the
+// stream (only when that kernel is this call's own transpose).
+cudaError_t launch_spmm_rows(const Plan &p, const SpmmArgs &a, bool pdl, cudaStream_t s);
+cudaError_t launch_spmm_cols(const Plan &p, const SpmmArgs &a, bool pdl, cudaStream_t s);
+cudaError_t launch_sddmm(const Plan &p, const SddmmArgs &a, bool pdl, cudaStream_t s);
+cudaError_t launch_backward_fused(const Plan &pc, const SpmmArgs &cols, const Plan &pr,
+                                  const SddmmArgs &rows, bool pdl, cudaStream_t s);
+// at[c * bw + b] = a[b * a_ld + c] and bt likewise, in one launch.
+cudaError_t launch_transpose_pair(const float *a, int64_t a_ld, int64_t a_cols, float *at,
+                                  const float *b, int64_t b_ld, int64_t b_cols, float *bt, int nb,
+                                  int bw, cudaStream_t s);
 // dst[c * bw + b] = b < nb ? src[b * ld + c] : 0, for c < ncols, b < bw.
 cudaError_t launch_transpose(const float *src, int64_t ld, int nb, int64_t ncols, float *dst,
                              int bw, cudaStream_t s);

@@ -1,23 +1,18 @@
-// Batch-width / team-size dispatch of the segmented kernels.  Each launcher
-// is instantiated in its own translation unit so the three families compile
-// in parallel.
+// Launch helpers for the segmented kernels: persistent grid sizing and
+// programmatic dependent launch.  Each kernel family is instantiated for the
+// seven slice widths in its own translation unit, so they compile in
+// parallel.
 #pragma once
 
 #include <mutex>
 #include <unordered_map>
+#include <utility>
 
 #include "spmm_kernels.cuh"
 
 namespace snack {
 
-// Lanes per entry for a slice width.  One 16-byte vector per lane, and the
-// G lanes of a group read an entry's whole dense row (up to one 128-byte
-// line) in ONE instruction: the L1 data pipe spends a wavefront per
-// (instruction, line), so splitting a row over several instructions costs
-// proportionally more.  BW = 64 (two lines) uses 8 lanes x 2 vectors.
-constexpr int lanes_for(int bw) { return bw <= 4 ? 1 : (bw >= 32 ? 8 : bw / 4); }
-
-// Resident blocks per SM of a kernel instantiation (queried once per kernel).
+// Resident blocks per SM of a kernel (queried once per kernel).
 inline int resident_blocks(const void *kern) {
   static std::mutex mu;
   static std::unordered_map<const void *, int> cache;
@@ -44,42 +39,68 @@ inline int sm_count() {
   return cached[dev];
 }
 
-// Persistent launch: no more blocks than can be resident at once.
-template <typename Args, typename Kern>
-inline cudaError_t launch_teams(Kern kern, const Args &a, int lps, cudaStream_t s) {
-  if (a.nseg == 0) return cudaSuccess;
-  const int64_t need = (a.nseg * (int64_t)lps + 255) / 256;
-  const int64_t cap = (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void *>(kern));
-  const int64_t grid = need < cap ? need : cap;
-  kern<<<(unsigned)grid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+// Blocks of a persistent grid: no more than can be resident at once.
+template <typename K>
+inline int64_t resident_capacity(K kern) {
+  return (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void *>(kern));
 }
 
-#define SNACK_TEAM_CASES(KERNEL, BW, ...)                                              \
-  switch (p.lanes < lanes_for(BW) ? lanes_for(BW) : p.lanes) {                         \
-    case 4:                                                                            \
-      return launch_teams(KERNEL<BW, lanes_for(BW), (lanes_for(BW) > 4 ? lanes_for(BW) : 4) __VA_ARGS__>, a, (lanes_for(BW) > 4 ? lanes_for(BW) : 4), s); \
-    case 8:                                                                            \
-      return launch_teams(KERNEL<BW, lanes_for(BW), 8 __VA_ARGS__>, a, 8, s);          \
-    case 16:                                                                           \
-      return launch_teams(KERNEL<BW, lanes_for(BW), 16 __VA_ARGS__>, a, 16, s);        \
-    case 32:                                                                           \
-      return launch_teams(KERNEL<BW, lanes_for(BW), 32 __VA_ARGS__>, a, 32, s);        \
-    default:                                                                           \
-      return cudaErrorInvalidValue;                                                    \
+// Launch with 256 threads.  pdl: the launch may begin while the previous
+// kernel on the stream is still running; the kernel's griddep_wait() holds
+// it until that kernel has completed and its writes are visible.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kern)(KArgs...), int64_t grid, bool pdl, cudaStream_t s,
+                             Args &&...args) {
+  if (grid < 1) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Team sizes are compiled for 8, 16 and 32 lanes.
+inline int team_lanes(const Plan &p) {
+  int l = p.lanes < lanes_for(p.bw) ? lanes_for(p.bw) : p.lanes;
+  return l < 8 ? 8 : (l > 32 ? 32 : l);
+}
+
+#define SNACK_BW_SWITCH(bw, CALL) \
+  switch (bw) {                   \
+    case 1: CALL(1)               \
+    case 2: CALL(2)               \
+    case 4: CALL(4)               \
+    case 8: CALL(8)               \
+    case 16: CALL(16)             \
+    case 32: CALL(32)             \
+    case 64: CALL(64)             \
+    default:                      \
+      return cudaErrorInvalidValue; \
   }
 
-#define SNACK_WIDTH_CASES(KERNEL, ...)              \
-  switch (p.bw) {                                   \
-    case 1: SNACK_TEAM_CASES(KERNEL, 1, __VA_ARGS__)   \
-    case 2: SNACK_TEAM_CASES(KERNEL, 2, __VA_ARGS__)   \
-    case 4: SNACK_TEAM_CASES(KERNEL, 4, __VA_ARGS__)   \
-    case 8: SNACK_TEAM_CASES(KERNEL, 8, __VA_ARGS__)   \
-    case 16: SNACK_TEAM_CASES(KERNEL, 16, __VA_ARGS__) \
-    case 32: SNACK_TEAM_CASES(KERNEL, 32, __VA_ARGS__) \
-    case 64: SNACK_TEAM_CASES(KERNEL, 64, __VA_ARGS__) \
-    default:                                        \
-      return cudaErrorInvalidValue;                 \
+// CALL2(W, L) for the slice width and team size of a plan.
+#define SNACK_BW_LPS_SWITCH(bw, lps, CALL2)                                   \
+  switch (bw * 64 + lps) {                                                    \
+    case 1 * 64 + 8: CALL2(1, 8) case 1 * 64 + 16: CALL2(1, 16)               \
+    case 1 * 64 + 32: CALL2(1, 32) case 2 * 64 + 8: CALL2(2, 8)               \
+    case 2 * 64 + 16: CALL2(2, 16) case 2 * 64 + 32: CALL2(2, 32)             \
+    case 4 * 64 + 8: CALL2(4, 8) case 4 * 64 + 16: CALL2(4, 16)               \
+    case 4 * 64 + 32: CALL2(4, 32) case 8 * 64 + 8: CALL2(8, 8)               \
+    case 8 * 64 + 16: CALL2(8, 16) case 8 * 64 + 32: CALL2(8, 32)             \
+    case 16 * 64 + 8: CALL2(16, 8) case 16 * 64 + 16: CALL2(16, 16)           \
+    case 16 * 64 + 32: CALL2(16, 32) case 32 * 64 + 8: CALL2(32, 8)           \
+    case 32 * 64 + 16: CALL2(32, 16) case 32 * 64 + 32: CALL2(32, 32)         \
+    case 64 * 64 + 8: CALL2(64, 8) case 64 * 64 + 16: CALL2(64, 16)           \
+    case 64 * 64 + 32: CALL2(64, 32)                                          \
+    default:                                                                  \
+      return cudaErrorInvalidValue;                                           \
   }
 
 }  // namespace snack

@@ -7,15 +7,17 @@
 // call whatever the batch:
 //
 //  * Entries are ordered by line (row for Y = X W^T and dW, column for
-//    dX = dY W) and each line is cut into segments.  A TEAM of LPS lanes owns
-//    one segment; inside a team, GROUPS of G lanes each take one entry at a
-//    time, and the G lanes of a group split the batch slice (BW floats,
+//    dX = dY W) and each line is cut into segments.  A TEAM of LPS lanes
+//    owns one segment; inside a team, GROUPS of G lanes each take one entry
+//    at a time, and the G lanes of a group split the batch slice (BW floats,
 //    16-byte vectors).  Each group walks 4 consecutive entries per step from
 //    one 16-byte load of indices and one of values (aligned down to a
-//    multiple of 4 and masked at the segment ends).
+//    multiple of 4 and masked at the segment ends), two such quads in flight.
 //  * The dense operand is gathered from a transposed copy (line-major,
-//    [lines][BW]) so that the BW batch values of one column are contiguous:
-//    one 32..256-byte run per entry instead of BW scattered words.
+//    [lines][BW]) so that the BW batch values of one column are contiguous.
+//    A group reads an entry's whole row (up to one 128-byte line) with ONE
+//    instruction: the L1 data pipe spends a wavefront per (instruction,
+//    line), so splitting a row across instructions multiplies its cost.
 //  * Partial sums of the groups are combined with warp shuffles; only lines
 //    split into several segments (long rows / columns) meet across warps,
 //    and they do it deterministically: each segment stores its partial, the
@@ -23,6 +25,10 @@
 //    writes the output, then re-arms the ticket.  No floating-point atomics.
 //  * Index and value streams bypass L1 (ld.global.nc.L1::no_allocate) so
 //    that L1 keeps the gathered dense rows.
+//  * Grids are persistent (resident blocks only) with a warp-uniform segment
+//    loop.  A kernel may be launched as a programmatic dependent of the
+//    transpose that feeds it: it waits (griddepcontrol.wait) before reading
+//    anything, so only its launch and block start-up overlap the producer.
 #pragma once
 
 #include "snack_internal.cuh"
@@ -45,9 +51,21 @@ __device__ __forceinline__ float4 ld_stream_f4(const float *p) {
   return r;
 }
 
+// Programmatic dependent launch: wait for the preceding grid (no-op when the
+// kernel was launched without the attribute) / let the next grid launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Lanes per entry for a slice width: one 16-byte vector per lane and the
+// whole row (up to 128 B) in one instruction; BW = 64 uses 8 lanes x 2.
+__host__ __device__ constexpr int lanes_for(int bw) { return bw <= 4 ? 1 : (bw >= 32 ? 8 : bw / 4); }
+
 // Shape of a batch slice: each lane holds NV vectors of VEC floats.
-template <int BW, int G>
+template <int BW>
 struct SliceShape {
+  static constexpr int G = lanes_for(BW);
   static constexpr int VEC = BW >= 4 ? 4 : BW;
   static constexpr int NV = BW >= 4 ? BW / (4 * G) : 1;
   static_assert(BW < 4 ? G == 1 : (BW % (4 * G) == 0), "bad slice shape");
@@ -78,22 +96,22 @@ __device__ __forceinline__ void load_vec<1>(const float *p, float (&x)[1]) {
 }
 
 // Lane (group 0, sub) holds batch b = v*G*VEC + sub*VEC + i.
-template <int BW, int G>
-__device__ __forceinline__ void store_line(const SpmmArgs &a, int line, int sub,
-                                           const float (&r)[SliceShape<BW, G>::NV]
-                                                           [SliceShape<BW, G>::VEC]) {
-  using S = SliceShape<BW, G>;
+template <int BW>
+__device__ __forceinline__ void store_line(float *dst, int64_t ld, int nb, int line, int sub,
+                                           const float (&r)[SliceShape<BW>::NV]
+                                                           [SliceShape<BW>::VEC]) {
+  using S = SliceShape<BW>;
 #pragma unroll
   for (int v = 0; v < S::NV; ++v)
 #pragma unroll
     for (int i = 0; i < S::VEC; ++i) {
-      const int b = v * G * S::VEC + sub * S::VEC + i;
-      if (b < a.nb) a.dst[(int64_t)b * a.ld + line] = r[v][i];
+      const int b = v * S::G * S::VEC + sub * S::VEC + i;
+      if (b < nb) dst[(int64_t)b * ld + line] = r[v][i];
     }
 }
 
 // Entries [kb, kb+4) of one group: indices / values from one 16-byte load
-// each, masked to the segment [k0, k1).
+// each; values of a column-order stream come through the permutation.
 template <bool PERM>
 __device__ __forceinline__ void load_quad(const SpmmArgs &a, int kb, int k0, int k1, int (&c)[4],
                                           float (&w)[4]) {
@@ -117,15 +135,14 @@ __device__ __forceinline__ void load_quad(const SpmmArgs &a, int kb, int k0, int
   }
 }
 
-// Gather the lane's slice of the dense rows of up to 8 entries (all loads
-// issued before any use), then accumulate.
-template <int BW, int G, int Q>
+// Gather the lane's slice of the dense rows of Q quads (all loads issued
+// before any use), then accumulate.
+template <int BW, int Q>
 __device__ __forceinline__ void gather_fma(const float *src, const int (&c)[Q][4],
                                            const float (&w)[Q][4], const bool (&ok)[Q][4],
-                                           float (&acc)[SliceShape<BW, G>::NV]
-                                                       [SliceShape<BW, G>::VEC]) {
-  using S = SliceShape<BW, G>;
-  constexpr int VEC = S::VEC, NV = S::NV;
+                                           float (&acc)[SliceShape<BW>::NV][SliceShape<BW>::VEC]) {
+  using S = SliceShape<BW>;
+  constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
   float x[Q][4][NV][VEC];
 #pragma unroll
   for (int q = 0; q < Q; ++q)
@@ -150,23 +167,24 @@ __device__ __forceinline__ void gather_fma(const float *src, const int (&c)[Q][4
         for (int i = 0; i < VEC; ++i) acc[v][i] = fmaf(w[q][e], x[q][e][v][i], acc[v][i]);
 }
 
-// One team of LPS lanes per segment; PERM = values reached through a
-// column-order -> canonical permutation (the dX = dY W direction).  The grid
-// is persistent: teams stride over the segments in a warp-uniform loop so
-// that the warp-wide shuffles always see every lane.
-template <int BW, int G, int LPS, bool PERM>
-__global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
-  using S = SliceShape<BW, G>;
-  constexpr int VEC = S::VEC, NV = S::NV, NPT = LPS / G;
+// Segmented SpMM over blocks [block, ...) of a persistent grid of `nblocks`.
+// PERM = values reached through a column-order -> canonical permutation
+// (the dX = dY W direction).
+template <int BW, int LPS, bool PERM>
+__device__ __forceinline__ void spmm_part(const SpmmArgs &a, int64_t block, int64_t nblocks) {
+  using S = SliceShape<BW>;
+  constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
+  constexpr int lps = LPS;  // lanes per team: power of two in [G, 32]
+  constexpr int npt = lps / G;
   static_assert(LPS % G == 0 && LPS <= 32, "bad team");
   const int lane = threadIdx.x & 31;
-  const int tlane = lane % LPS;
+  const int tlane = lane & (lps - 1);
   const int grp = tlane / G;
   const int sub = tlane % G;
-  const int64_t teams_per_block = blockDim.x / LPS;
-  const int64_t stride = (int64_t)gridDim.x * teams_per_block;
-  const int64_t my_team = (int64_t)blockIdx.x * teams_per_block + threadIdx.x / LPS;
-  const int64_t warp_team = (int64_t)blockIdx.x * teams_per_block + (threadIdx.x & ~31) / LPS;
+  const int64_t teams_per_block = blockDim.x / lps;
+  const int64_t stride = nblocks * teams_per_block;
+  const int64_t my_team = block * teams_per_block + threadIdx.x / lps;
+  const int64_t warp_team = block * teams_per_block + (threadIdx.x & ~31) / lps;
   const float *src = a.src + sub * VEC;
 
   for (int64_t t0 = 0; warp_team + t0 < a.nseg; t0 += stride) {
@@ -183,20 +201,20 @@ __global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
       for (int i = 0; i < VEC; ++i) acc[v][i] = 0.f;
 
     int kb = (k0 & ~3) + 4 * grp;
-    for (; kb + 4 * NPT < k1; kb += 8 * NPT) {  // two quads in flight
+    for (; kb + 4 * npt < k1; kb += 8 * npt) {  // two quads in flight
       int c[2][4];
       float w[2][4];
       bool ok[2][4];
       load_quad<PERM>(a, kb, k0, k1, c[0], w[0]);
-      load_quad<PERM>(a, kb + 4 * NPT, k0, k1, c[1], w[1]);
+      load_quad<PERM>(a, kb + 4 * npt, k0, k1, c[1], w[1]);
 #pragma unroll
       for (int q = 0; q < 2; ++q)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int k = kb + q * 4 * NPT + e;
+          const int k = kb + q * 4 * npt + e;
           ok[q][e] = k >= k0 && k < k1;
         }
-      gather_fma<BW, G, 2>(src, c, w, ok, acc);
+      gather_fma<BW, 2>(src, c, w, ok, acc);
     }
     if (kb < k1) {
       int c[1][4];
@@ -205,12 +223,12 @@ __global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
       load_quad<PERM>(a, kb, k0, k1, c[0], w[0]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) ok[0][e] = kb + e >= k0 && kb + e < k1;
-      gather_fma<BW, G, 1>(src, c, w, ok, acc);
+      gather_fma<BW, 1>(src, c, w, ok, acc);
     }
 
-    // Combine the NPT groups of the team (every lane of the warp is here).
+    // Combine the npt groups of the team (every lane of the warp is here).
 #pragma unroll
-    for (int off = G; off < LPS; off <<= 1)
+    for (int off = G; off < lps; off <<= 1)
 #pragma unroll
       for (int v = 0; v < NV; ++v)
 #pragma unroll
@@ -219,7 +237,7 @@ __global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
     if (!active) continue;
     const int line = sg.x;
     if (sg.w < 0) {
-      if (grp == 0) store_line<BW, G>(a, line, sub, acc);
+      if (grp == 0) store_line<BW>(a.dst, a.ld, a.nb, line, sub, acc);
       continue;
     }
 
@@ -234,7 +252,7 @@ __global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
         for (int i = 0; i < VEC; ++i) mine[v * G * VEC + i] = acc[v][i];
     }
     __threadfence();
-    const unsigned tmask = LPS == 32 ? 0xffffffffu : (((1u << LPS) - 1u) << (lane - tlane));
+    const unsigned tmask = lps == 32 ? 0xffffffffu : (((1u << lps) - 1u) << (lane - tlane));
     __syncwarp(tmask);
     int last = 0;
     if (tlane == 0) last = atomicAdd(a.counter + sg.w, 1) == sp.y - 1;
@@ -254,23 +272,22 @@ __global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
 #pragma unroll
           for (int i = 0; i < VEC; ++i) tot[v][i] += __ldcg(q + v * G * VEC + i);
       }
-      store_line<BW, G>(a, line, sub, tot);
+      store_line<BW>(a.dst, a.ld, a.nb, line, sub, tot);
     }
     if (tlane == 0) a.counter[sg.w] = 0;  // re-arm for the next call
   }
 }
 
-// dW[k] = sum_b dY[b][row_k] X[b][col_k] over the row segments; the G lanes
-// of a group each form part of the batch dot product and meet by shuffle.
-// Persistent grid; a team's lanes stay together, groups never diverge.
-template <int BW, int G>
+// dW for up to two quads of one group: the G lanes of a group each form part
+// of the batch dot product and meet by shuffle.
+template <int BW>
 __device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt, int kb, int k0,
                                             int k1, int npt, unsigned gmask, int sub,
-                                            const float (&dy)[SliceShape<BW, G>::NV]
-                                                             [SliceShape<BW, G>::VEC],
+                                            const float (&dy)[SliceShape<BW>::NV]
+                                                             [SliceShape<BW>::VEC],
                                             bool two) {
-  using S = SliceShape<BW, G>;
-  constexpr int VEC = S::VEC, NV = S::NV;
+  using S = SliceShape<BW>;
+  constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
   int c[2][4];
   float x[2][4][NV][VEC];
 #pragma unroll
@@ -335,20 +352,24 @@ __device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt,
   }
 }
 
-template <int BW, int G, int LPS>
-__global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
-  using S = SliceShape<BW, G>;
-  constexpr int VEC = S::VEC, NV = S::NV, NPT = LPS / G;
+// dW[k] = sum_b dY[b][row_k] X[b][col_k] over the row segments (persistent
+// grid of `nblocks`; a team's lanes stay together, groups never diverge).
+template <int BW, int LPS>
+__device__ __forceinline__ void sddmm_part(const SddmmArgs &a, int64_t block, int64_t nblocks) {
+  using S = SliceShape<BW>;
+  constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
+  constexpr int lps = LPS;
+  constexpr int npt = lps / G;
+  static_assert(LPS % G == 0 && LPS <= 32, "bad team");
   const int lane = threadIdx.x & 31;
-  const int tlane = lane % LPS;
+  const int tlane = lane & (lps - 1);
   const int grp = tlane / G;
   const int sub = tlane % G;
   const unsigned gmask = G == 1 ? (1u << lane) : (((1u << G) - 1u) << (lane & ~(G - 1)));
-  const int64_t teams_per_block = blockDim.x / LPS;
-  const int64_t stride = (int64_t)gridDim.x * teams_per_block;
+  const int64_t teams_per_block = blockDim.x / lps;
+  const int64_t stride = nblocks * teams_per_block;
   const float *xt = a.xt + sub * VEC;
-  for (int64_t team = (int64_t)blockIdx.x * teams_per_block + threadIdx.x / LPS; team < a.nseg;
-       team += stride) {
+  for (int64_t team = block * teams_per_block + threadIdx.x / lps; team < a.nseg; team += stride) {
     const int4 sg = a.seg[team];
     const int r = sg.x, k0 = sg.y, k1 = sg.z;
     float dy[NV][VEC];
@@ -358,29 +379,78 @@ __global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
       for (int v = 0; v < NV; ++v) load_vec<VEC>(p + v * G * VEC, dy[v]);
     }
     int kb = (k0 & ~3) + 4 * grp;
-    for (; kb + 4 * NPT < k1; kb += 8 * NPT)
-      sddmm_quads<BW, G>(a, xt, kb, k0, k1, NPT, gmask, sub, dy, true);
-    if (kb < k1) sddmm_quads<BW, G>(a, xt, kb, k0, k1, NPT, gmask, sub, dy, false);
+    for (; kb + 4 * npt < k1; kb += 8 * npt)
+      sddmm_quads<BW>(a, xt, kb, k0, k1, npt, gmask, sub, dy, true);
+    if (kb < k1) sddmm_quads<BW>(a, xt, kb, k0, k1, npt, gmask, sub, dy, false);
   }
 }
 
-// dst[c * BW + b] = b < nb ? src[b * ld + c] : 0  (32 columns per block).
+template <int BW, int LPS, bool PERM>
+__global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
+  griddep_wait();
+  spmm_part<BW, LPS, PERM>(a, blockIdx.x, gridDim.x);
+}
+
+template <int BW, int LPS>
+__global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
+  griddep_wait();
+  sddmm_part<BW, LPS>(a, blockIdx.x, gridDim.x);
+}
+
+// Both backward products in one launch: the first `cols_blocks` blocks run
+// dX over the column segments, the rest run dW over the row segments (one
+// team size for both parts).
+template <int BW, int LPS>
+__global__ void __launch_bounds__(256) backward_segments(const SpmmArgs cols, const SddmmArgs rows,
+                                                         int cols_blocks) {
+  griddep_wait();
+  if ((int)blockIdx.x < cols_blocks)
+    spmm_part<BW, LPS, true>(cols, blockIdx.x, cols_blocks);
+  else
+    sddmm_part<BW, LPS>(rows, blockIdx.x - cols_blocks, gridDim.x - cols_blocks);
+}
+
+// dst[c * BW + b] = b < nb ? src[b * ld + c] : 0 for 32 columns per block.
 template <int BW>
-__global__ void __launch_bounds__(256) transpose_pad(const float *__restrict__ src, int64_t ld,
-                                                     int nb, int64_t ncols,
-                                                     float *__restrict__ dst) {
-  __shared__ float tile[BW][33];
+__device__ __forceinline__ void transpose_tile(const float *__restrict__ src, int64_t ld, int nb,
+                                               int64_t ncols, float *__restrict__ dst, int64_t tile,
+                                               float (*buf)[33]) {
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int64_t c0 = (int64_t)blockIdx.x * 32;
+  const int64_t c0 = tile * 32;
   for (int b = ty; b < BW; b += 8) {
     const int64_t c = c0 + tx;
-    tile[b][tx] = (b < nb && c < ncols) ? src[(int64_t)b * ld + c] : 0.f;
+    buf[b][tx] = (b < nb && c < ncols) ? src[(int64_t)b * ld + c] : 0.f;
   }
   __syncthreads();
   for (int f = threadIdx.x; f < 32 * BW; f += 256) {
     const int cc = f / BW, b = f % BW;
-    if (c0 + cc < ncols) dst[(c0 + cc) * BW + b] = tile[b][cc];
+    if (c0 + cc < ncols) dst[(c0 + cc) * BW + b] = buf[b][cc];
   }
+}
+
+template <int BW>
+__global__ void __launch_bounds__(256) transpose_pad(const float *__restrict__ src, int64_t ld,
+                                                     int nb, int64_t ncols,
+                                                     float *__restrict__ dst) {
+  __shared__ float buf[BW][33];
+  griddep_launch();
+  transpose_tile<BW>(src, ld, nb, ncols, dst, blockIdx.x, buf);
+}
+
+// Two transposes in one launch (X for dW, dY for dX and dW): the first
+// `a_tiles` blocks handle a, the rest b.
+template <int BW>
+__global__ void __launch_bounds__(256) transpose_pair(const float *__restrict__ a, int64_t a_ld,
+                                                      int64_t a_cols, float *__restrict__ at,
+                                                      const float *__restrict__ b, int64_t b_ld,
+                                                      int64_t b_cols, float *__restrict__ bt,
+                                                      int nb, int64_t a_tiles) {
+  __shared__ float buf[BW][33];
+  griddep_launch();
+  if ((int64_t)blockIdx.x < a_tiles)
+    transpose_tile<BW>(a, a_ld, nb, a_cols, at, blockIdx.x, buf);
+  else
+    transpose_tile<BW>(b, b_ld, nb, b_cols, bt, blockIdx.x - a_tiles, buf);
 }
 
 }  // namespace snack

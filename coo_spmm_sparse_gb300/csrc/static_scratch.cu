@@ -43,6 +43,7 @@ struct CsrStaticArgs {
   float *dst;        // Y, element (b, row) at dst[b * ld + row]
   int64_t ld;
   int nb;
+  int lps;
 };
 
 __device__ __forceinline__ void load_quad_bounded(const CsrStaticArgs &a, int kb, int (&c)[4],
@@ -68,19 +69,20 @@ __device__ __forceinline__ void load_quad_bounded(const CsrStaticArgs &a, int kb
   }
 }
 
-template <int BW, int G, int LPS>
+template <int BW>
 __global__ void __launch_bounds__(256) spmm_csr_rows_static(const CsrStaticArgs a) {
-  using S = SliceShape<BW, G>;
-  constexpr int VEC = S::VEC, NV = S::NV, NPT = LPS / G;
-  static_assert(LPS % G == 0 && LPS <= 32, "bad team");
+  using S = SliceShape<BW>;
+  constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
+  const int lps = a.lps;  // power of two in [G, 32]
+  const int npt = lps / G;
   const int lane = threadIdx.x & 31;
-  const int tlane = lane % LPS;
+  const int tlane = lane & (lps - 1);
   const int grp = tlane / G;
   const int sub = tlane % G;
-  const int64_t teams_per_block = blockDim.x / LPS;
+  const int64_t teams_per_block = blockDim.x / lps;
   const int64_t stride = (int64_t)gridDim.x * teams_per_block;
-  const int64_t my_team = (int64_t)blockIdx.x * teams_per_block + threadIdx.x / LPS;
-  const int64_t warp_team = (int64_t)blockIdx.x * teams_per_block + (threadIdx.x & ~31) / LPS;
+  const int64_t my_team = (int64_t)blockIdx.x * teams_per_block + threadIdx.x / lps;
+  const int64_t warp_team = (int64_t)blockIdx.x * teams_per_block + (threadIdx.x & ~31) / lps;
   const float *src = a.src + sub * VEC;
 
   for (int64_t t0 = 0; warp_team + t0 < a.nseg; t0 += stride) {
@@ -95,18 +97,17 @@ __global__ void __launch_bounds__(256) spmm_csr_rows_static(const CsrStaticArgs 
 #pragma unroll
       for (int i = 0; i < VEC; ++i) acc[v][i] = 0.f;
 
-    for (int kb = (k0 & ~3) + 4 * grp; kb < k1; kb += 4 * NPT) {
+    for (int kb = (k0 & ~3) + 4 * grp; kb < k1; kb += 4 * npt) {
       int c[1][4];
       float w[1][4];
       bool ok[1][4];
       load_quad_bounded(a, kb, c[0], w[0]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) ok[0][e] = kb + e >= k0 && kb + e < k1;
-      gather_fma<BW, G, 1>(src, c, w, ok, acc);
+      gather_fma<BW, 1>(src, c, w, ok, acc);
     }
 
-#pragma unroll
-    for (int off = G; off < LPS; off <<= 1)
+    for (int off = G; off < lps; off <<= 1)
 #pragma unroll
       for (int v = 0; v < NV; ++v)
 #pragma unroll
@@ -124,8 +125,18 @@ __global__ void __launch_bounds__(256) spmm_csr_rows_static(const CsrStaticArgs 
   }
 }
 
-cudaError_t launch_csr_rows_static(const Plan &p, const CsrStaticArgs &a, cudaStream_t s) {
-  SNACK_WIDTH_CASES(spmm_csr_rows_static, )
+cudaError_t launch_csr_rows_static(const Plan &p, const CsrStaticArgs &args, cudaStream_t s) {
+  CsrStaticArgs a = args;
+  a.lps = team_lanes(p);
+  const int64_t need = (a.nseg * a.lps + 255) / 256;
+#define SNACK_CALL(W)                                                        \
+  {                                                                          \
+    auto k = spmm_csr_rows_static<W>;                                        \
+    const int64_t cap = resident_capacity(k);                                \
+    return launch_ex(k, need < cap ? need : cap, false, s, a);               \
+  }
+  SNACK_BW_SWITCH(p.bw, SNACK_CALL)
+#undef SNACK_CALL
 }
 
 snack_status fail(snack_status st, const std::string &msg) {

@@ -261,7 +261,7 @@ def test_plan_follows_batch_and_row_length():
     small = workloads.workload("toy256").layers[0]
     r, c, v = small.coo()
     h2 = sn().snack_create(small.out, small.inp, r, c, v)
-    assert sn().snack_plan(h2, 0, 4)[1] == 4             # ~26 entries per row
+    assert sn().snack_plan(h2, 0, 4)[1] == 8             # ~26 entries per row
 
 
 # ------------------------------------------------------------ Algorithm 2
