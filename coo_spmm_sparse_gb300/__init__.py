@@ -33,7 +33,7 @@ __all__ = [
     "SnackError", "SnackHandle", "snack_create", "snack_create_random", "snack_forward",
     "snack_backward_input", "snack_backward_weight", "snack_backward", "snack_prune_regrow",
     "snack_values", "snack_export", "snack_export_segments", "snack_plan", "snack_nnz",
-    "snack_device_bytes", "snack_destroy", "snack_launch_count", "snack_forward_csr_static", "SnackLinear", "library_path",
+    "snack_device_bytes", "snack_destroy", "snack_launch_count", "snack_forward_csr_static", "snack_device_error", "SnackLinear", "library_path",
 ]
 
 
@@ -249,10 +249,14 @@ def snack_export_segments(h: SnackHandle):
     return res
 
 
-def snack_plan(h: SnackHandle, op: int, batch: int):
-    """(slice_width, lanes_per_segment, segments) chosen for op 0/1/2 at this batch."""
-    w, l, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
-    _check(_lib.snack_plan(h.ptr, op, batch, ctypes.byref(w), ctypes.byref(l), ctypes.byref(s)), h)
+def snack_plan(h: SnackHandle, op: int, batch: int, with_tiles: bool = False):
+    """(slice_width, lanes_per_segment, segments[, tile_cols]) chosen for op
+    0/1/2 at this batch; tile_cols = 0 means the segmented kernel runs."""
+    w, l, s, t = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int32()
+    _check(_lib.snack_plan(h.ptr, op, batch, ctypes.byref(w), ctypes.byref(l), ctypes.byref(s),
+                           ctypes.byref(t)), h)
+    if with_tiles:
+        return int(w.value), int(l.value), int(s.value), int(t.value)
     return int(w.value), int(l.value), int(s.value)
 
 
@@ -276,6 +280,13 @@ def snack_forward_csr_static(out: int, inp: int, row_ptr: torch.Tensor, col: tor
                                          _ptr(val) if nnz else None, _ptr(X), _ptr(Y), B,
                                          _stream(stream, X.device)))
     return Y
+
+
+def snack_device_error(h: SnackHandle) -> int:
+    """Read and clear the handle's device error flag (1 = a bounded wait gave up)."""
+    f = ctypes.c_int(0)
+    _check(_lib.snack_device_error(h.ptr, ctypes.byref(f), _stream(None)), h)
+    return int(f.value)
 
 
 def snack_launch_count() -> int:

@@ -29,9 +29,10 @@ SIGNATURES = {
     "snack_values": (ctypes.c_int, [vp, P(vp)]),
     "snack_export": (ctypes.c_int, [vp, vp, vp, vp, ctypes.c_int, vp]),
     "snack_export_segments": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
-    "snack_plan": (ctypes.c_int, [vp, ctypes.c_int, i64, P(i32), P(i32), P(i64)]),
+    "snack_plan": (ctypes.c_int, [vp, ctypes.c_int, i64, P(i32), P(i32), P(i64), P(i32)]),
     "snack_forward_csr_static": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp, vp, i64, vp]),
     "snack_launch_count": (u64, []),
+    "snack_device_error": (ctypes.c_int, [vp, P(ctypes.c_int), vp]),
     "snack_nnz": (i64, [vp]),
     "snack_out_features": (i64, [vp]),
     "snack_in_features": (i64, [vp]),

@@ -72,6 +72,7 @@ void account(snack::Layer &L) {
   b += (size_t)(L.in + L.out) * snack::kMaxSlice * 4;
   b += (size_t)std::max(L.csr.nslots, L.csc.nslots) * snack::kMaxSlice * 4;
   b += (size_t)std::max(L.csr.nsplit, L.csc.nsplit) * 4;
+  b += (size_t)(L.pan_csr.ncta + 1 + L.pan_csc.ncta + 1) * 4 + 4;  // panels, error flag
   L.device_bytes = b;
 }
 
@@ -103,6 +104,7 @@ snack::SpmmArgs spmm_args(snack::Layer &L, bool rows, const float *op, float *ds
   a.partial = L.d_partial;
   a.counter = L.d_counter;
   a.lps = 32;
+  a.nval = L.nnz_pad;
   return a;
 }
 
@@ -388,7 +390,7 @@ snack_status snack_export_segments(snack_handle h, int32_t *row_ptr, int32_t *co
 }
 
 snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_width,
-                        int32_t *lanes_per_segment, int64_t *segments) {
+                        int32_t *lanes_per_segment, int64_t *segments, int32_t *tile_cols) {
   if (!h) return fail(nullptr, SNACK_ERR_INVALID_ARG, "handle is NULL");
   if (op < 0 || op > 2 || batch < 1) return fail(h, SNACK_ERR_INVALID_ARG, "bad op or batch");
   const snack::SegTable &t = op == 1 ? h->L.csc : h->L.csr;
@@ -396,10 +398,24 @@ snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_wi
   if (slice_width) *slice_width = p.bw;
   if (lanes_per_segment) *lanes_per_segment = p.lanes;
   if (segments) *segments = t.nseg;
+  if (tile_cols) *tile_cols = 0;  // every op runs the segmented kernels
   return SNACK_OK;
 }
 
 uint64_t snack_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+snack_status snack_device_error(snack_handle h, int *flag, void *stream) {
+  if (!h || !flag) return fail(h, SNACK_ERR_INVALID_ARG, "NULL argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(&v, h->L.d_err, sizeof(int), cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+      (e = cudaMemsetAsync(h->L.d_err, 0, sizeof(int), s)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(s)) != cudaSuccess)
+    return cuda_fail(h, e, "reading the device error flag");
+  *flag = v;
+  return SNACK_OK;
+}
 
 int64_t snack_nnz(snack_handle h) { return h ? h->L.nnz : -1; }
 int64_t snack_out_features(snack_handle h) { return h ? h->L.out : -1; }

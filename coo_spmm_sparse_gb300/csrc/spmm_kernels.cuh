@@ -51,6 +51,43 @@ __device__ __forceinline__ float4 ld_stream_f4(const float *p) {
   return r;
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, multiple of 16).
+__device__ __forceinline__ void l2_prefetch(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Each team's first lane asks L2 for the index (and value or permutation)
+// ranges of every segment the team will process, so that the walk over them
+// hits L2 instead of paying a DRAM round trip per step.  Segment ranges are
+// rounded out to 16 bytes (the streams are padded).
+__device__ __forceinline__ void prefetch_segments(const int4 *seg, int64_t nseg, const int32_t *a,
+                                                  const void *b, int lps, int64_t block,
+                                                  int64_t nblocks) {
+  const int64_t teams_per_block = blockDim.x / lps;
+  if ((threadIdx.x & (lps - 1)) != 0) return;
+  for (int64_t t = block * teams_per_block + threadIdx.x / lps; t < nseg;
+       t += nblocks * teams_per_block) {
+    const int4 sg = seg[t];
+    const int k0 = sg.y & ~3, k1 = (sg.z + 3) & ~3;
+    if (k1 <= k0) continue;
+    l2_prefetch(a + k0, (uint32_t)(k1 - k0) * 4);
+    if (b) l2_prefetch(static_cast<const int32_t *>(b) + k0, (uint32_t)(k1 - k0) * 4);
+  }
+}
+
+// Ask L2 for this block's share of a whole array (the values reached through
+// the column permutation are read at random).
+__device__ __forceinline__ void prefetch_share(const float *p, int64_t n, int64_t block,
+                                               int64_t nblocks) {
+  if (threadIdx.x != 0 || n <= 0) return;
+  const int64_t per = (((n + nblocks - 1) / nblocks) + 3) & ~int64_t(3);
+  const int64_t b0 = block * per;
+  if (b0 >= n) return;
+  const int64_t len = (b0 + per < n ? per : ((n - b0 + 3) & ~int64_t(3)));
+  for (int64_t off = 0; off < len; off += 8192)
+    l2_prefetch(p + b0 + off, (uint32_t)((len - off < 8192 ? len - off : 8192) * 4));
+}
+
 // Programmatic dependent launch: wait for the preceding grid (no-op when the
 // kernel was launched without the attribute) / let the next grid launch.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -164,7 +201,10 @@ __device__ __forceinline__ void gather_fma(const float *src, const int (&c)[Q][4
 #pragma unroll
       for (int v = 0; v < NV; ++v)
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) acc[v][i] = fmaf(w[q][e], x[q][e][v][i], acc[v][i]);
+        for (int i = 0; i < VEC; ++i)
+          // masked entries (a neighbouring line's) add exactly nothing, even
+          // when their value is infinite or NaN
+          acc[v][i] = fmaf(ok[q][e] ? w[q][e] : 0.f, x[q][e][v][i], acc[v][i]);
 }
 
 // Segmented SpMM over blocks [block, ...) of a persistent grid of `nblocks`.
@@ -387,12 +427,18 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, int64_t block, in
 
 template <int BW, int LPS, bool PERM>
 __global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
+  // Index / value streams do not depend on the transpose this kernel may
+  // follow: start pulling them into L2 before waiting for it.
+  prefetch_segments(a.seg, a.nseg, a.idx, PERM ? (const void *)a.perm : (const void *)a.val, LPS,
+                    blockIdx.x, gridDim.x);
+  if (PERM) prefetch_share(a.val, a.nval, blockIdx.x, gridDim.x);
   griddep_wait();
   spmm_part<BW, LPS, PERM>(a, blockIdx.x, gridDim.x);
 }
 
 template <int BW, int LPS>
 __global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
+  prefetch_segments(a.seg, a.nseg, a.col, nullptr, LPS, blockIdx.x, gridDim.x);
   griddep_wait();
   sddmm_part<BW, LPS>(a, blockIdx.x, gridDim.x);
 }
@@ -403,6 +449,13 @@ __global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
 template <int BW, int LPS>
 __global__ void __launch_bounds__(256) backward_segments(const SpmmArgs cols, const SddmmArgs rows,
                                                          int cols_blocks) {
+  if ((int)blockIdx.x < cols_blocks) {
+    prefetch_segments(cols.seg, cols.nseg, cols.idx, cols.perm, LPS, blockIdx.x, cols_blocks);
+    prefetch_share(cols.val, cols.nval, blockIdx.x, cols_blocks);
+  } else {
+    prefetch_segments(rows.seg, rows.nseg, rows.col, nullptr, LPS, blockIdx.x - cols_blocks,
+                      gridDim.x - cols_blocks);
+  }
   griddep_wait();
   if ((int)blockIdx.x < cols_blocks)
     spmm_part<BW, LPS, true>(cols, blockIdx.x, cols_blocks);

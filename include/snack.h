@@ -175,10 +175,12 @@ snack_status snack_export_segments(snack_handle h, int32_t *row_ptr, int32_t *co
  * Which kernel variant a call would run: for op 0 = forward, 1 =
  * backward_input, 2 = backward_weight and the given batch, returns the
  * batch slice width (1, 2, 4, 8, 16, 32 or 64), the lanes that share one
- * row (or column) segment, and the number of segments.  Pure host query.
+ * row (or column) segment, the number of segments, and the operand lines per
+ * shared-memory tile of the panel x tile kernel (0 when the segmented kernel
+ * runs instead).  Any output may be NULL.  Pure host query.
  */
 snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_width,
-                        int32_t *lanes_per_segment, int64_t *segments);
+                        int32_t *lanes_per_segment, int64_t *segments, int32_t *tile_cols);
 
 /*
  * Forward pass Y = X W^T for callers that cannot allocate device memory.
@@ -213,6 +215,15 @@ snack_status snack_forward_csr_static(int64_t out_features, int64_t in_features,
                                       const int32_t *row_ptr, const int32_t *col,
                                       const float *val, const float *X, float *Y,
                                       int64_t batch, void *stream);
+
+/*
+ * Read and clear the handle's device error flag: *flag = 1 if, since the
+ * last read, a kernel of this handle gave up a bounded wait on one of its
+ * own shared-memory copies (its outputs for that call are then not to be
+ * trusted); 0 otherwise.  Kernels never trap or hang on such a failure.
+ * Synchronises `stream`.
+ */
+snack_status snack_device_error(snack_handle h, int *flag, void *stream);
 
 /*
  * Kernel launches this library has issued in the process so far (all

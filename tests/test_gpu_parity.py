@@ -139,6 +139,51 @@ def test_large99_full_oracle_b16():
     check_products(h, L.out, L.inp, ref, X, dY, fused=False)
 
 
+# ------------------------------------------------------------ dense-ish layer
+
+def test_dense_lines_full_oracle():
+    # 3000 x 3000 at 15 %: 1.35M entries, 450 per row and per column, every
+    # slice width, batch slices above 64 accumulating dW; full oracle.
+    out = inp = 3000
+    nnz = workloads.nnz_for(out, inp, 85)
+    row, col = workloads.uniform_pattern(out, inp, nnz, 11)
+    val = workloads.normal(nnz, 0.05, 11, 0)
+    ref = canonical(out, inp, row, col, val)
+    h = sn().snack_create(out, inp, row, col, val)
+    g = np.random.default_rng(12)
+    for B in (4, 8, 16, 33, 64, 70):
+        X = g.standard_normal((B, inp)).astype(np.float32)
+        dY = g.standard_normal((B, out)).astype(np.float32)
+        check_products(h, out, inp, ref, X, dY)
+    assert sn().snack_device_error(h) == 0
+
+
+def test_nonfinite_values_stay_in_their_lines():
+    # Entries with +-inf / NaN values poison only the outputs that sum them;
+    # neighbouring lines (whose 16-byte loads cover those entries) are exact.
+    g = np.random.default_rng(13)
+    for (out, inp, dens) in ((300, 200, 0.2), (3000, 3000, 0.15)):
+        nnz = workloads.nnz_for(out, inp, round(100 * (1 - dens)))
+        row, col = workloads.uniform_pattern(out, inp, nnz, 13)
+        val = workloads.normal(nnz, 1.0, 13, 0)
+        bad = g.choice(nnz, 5, replace=False)
+        val[bad] = np.array([np.inf, -np.inf, np.nan, np.inf, np.nan], np.float32)
+        ref = canonical(out, inp, row, col, val)
+        h = sn().snack_create(out, inp, row, col, val)
+        X = g.standard_normal((16, inp)).astype(np.float32)
+        dY = g.standard_normal((16, out)).astype(np.float32)
+        Y = sn().snack_forward(h, to_dev(X)).cpu().numpy()
+        dX = sn().snack_backward_input(h, to_dev(dY)).cpu().numpy()
+        Yo, Sy = oracle.forward(out, inp, ref["row"], ref["col"], ref["val"], X)
+        dXo, Sx = oracle.backward_input(out, inp, ref["row"], ref["col"], ref["val"], dY)
+        fin_r = np.isfinite(Sy).all(axis=0)
+        fin_c = np.isfinite(Sx).all(axis=0)
+        assert fin_r.sum() < out and fin_c.sum() < inp
+        assert_close("Y finite rows", Y[:, fin_r], Yo[:, fin_r], Sy[:, fin_r])
+        assert_close("dX finite cols", dX[:, fin_c], dXo[:, fin_c], Sx[:, fin_c])
+        assert not np.isfinite(Y[:, ~fin_r]).any()
+
+
 # ------------------------------------------------------------ edge cases
 
 def test_empty_layer_and_empty_lines():
