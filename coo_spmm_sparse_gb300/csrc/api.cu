@@ -125,7 +125,9 @@ snack_status run_forward(snack_handle h, const float *X, float *Y, int64_t batch
       op = L.d_xt;
     }
     const snack::SpmmArgs a = spmm_args(L, true, op, Y + b0 * L.out, nb);
-    cudaError_t e = snack::launch_spmm_rows(p, a, transposed, s);
+    cudaError_t e = snack::resident_fits(p.bw, L.in, L.csr.nseg)
+                        ? snack::launch_resident_spmm(false, p, a, L.in, L.d_err, transposed, s)
+                        : snack::launch_spmm_rows(p, a, transposed, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "forward launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }
@@ -166,6 +168,28 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     rows.lps = 32;
   }
   cudaError_t e;
+  const bool res_c = dX && snack::resident_fits(pc.bw, L.out, L.csc.nseg);
+  const bool res_r = dW && snack::resident_fits(pr.bw, L.in, L.csr.nseg);
+  if ((res_c || res_r) && (!(dX && dW) || L.nnz >= (int64_t(1) << 19))) {
+    // Operand resident in shared memory for at least one product (and, when
+    // both are wanted, a layer large enough that a second launch is cheap):
+    // one launch per product, the second waiting for the first.
+    bool pdl = transposed;
+    if (dX) {
+      e = res_c ? snack::launch_resident_spmm(true, pc, cols, L.out, L.d_err, pdl, s)
+                : snack::launch_spmm_cols(pc, cols, pdl, s);
+      if (e != cudaSuccess) return cuda_fail(h, e, "backward-input launch");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+      pdl = true;
+    }
+    if (dW) {
+      e = res_r ? snack::launch_resident_sddmm(pr, rows, L.in, L.d_err, pdl, s)
+                : snack::launch_sddmm(pr, rows, pdl, s);
+      if (e != cudaSuccess) return cuda_fail(h, e, "backward-weight launch");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    return SNACK_OK;
+  }
   if (dX && dW)
     e = snack::launch_backward_fused(pc, cols, pr, rows, transposed, s);
   else if (dX)

@@ -119,6 +119,14 @@ cudaError_t launch_spmm_cols(const Plan &p, const SpmmArgs &a, bool pdl, cudaStr
 cudaError_t launch_sddmm(const Plan &p, const SddmmArgs &a, bool pdl, cudaStream_t s);
 cudaError_t launch_backward_fused(const Plan &pc, const SpmmArgs &cols, const Plan &pr,
                                   const SddmmArgs &rows, bool pdl, cudaStream_t s);
+// Variants with the whole operand resident in shared memory (slices of 1-4
+// floats; resident_operand.cu).  n_op = operand lines (in for the forward
+// and dW, out for dX); err = the layer's device error flag.
+bool resident_fits(int bw, int64_t n_op, int64_t nseg);
+cudaError_t launch_resident_spmm(bool perm, const Plan &p, const SpmmArgs &a, int64_t n_op,
+                                 int *err, bool pdl, cudaStream_t s);
+cudaError_t launch_resident_sddmm(const Plan &p, const SddmmArgs &a, int64_t n_op, int *err,
+                                  bool pdl, cudaStream_t s);
 // at[c * bw + b] = a[b * a_ld + c] and bt likewise, in one launch.
 cudaError_t launch_transpose_pair(const float *a, int64_t a_ld, int64_t a_cols, float *at,
                                   const float *b, int64_t b_ld, int64_t b_cols, float *bt, int nb,

@@ -7,13 +7,9 @@ cudaError_t launch_spmm_cols(const Plan &p, const SpmmArgs &args, bool pdl, cuda
   if (args.nseg == 0) return cudaSuccess;
   SpmmArgs a = args;
   a.lps = team_lanes(p);
-  const int64_t need = (a.nseg * a.lps + 255) / 256;
-#define SNACK_CALL(W, L)                                        \
-  {                                                             \
-    auto k = spmm_segments<W, L, true>;                         \
-    const int64_t cap = resident_capacity(k);                   \
-    return launch_ex(k, need < cap ? need : cap, pdl, s, a);    \
-  }
+#define SNACK_CALL(W, L)                                                          \
+  return launch_one_wave(spmm_segments<W, L, true>, L,                           \
+                         spmm_segments<W, half_team(W, L), true>, half_team(W, L), a, pdl, s);
   SNACK_BW_LPS_SWITCH(p.bw, a.lps, SNACK_CALL)
 #undef SNACK_CALL
 }

@@ -85,6 +85,32 @@ inline int team_lanes(const Plan &p) {
       return cudaErrorInvalidValue; \
   }
 
+// Team size one step down from L for slice width W (L itself if none).
+constexpr int half_team(int W, int L) {
+  return (L / 2 >= 8 && L / 2 >= lanes_for(W)) ? L / 2 : L;
+}
+
+// Launch `k` (teams of L lanes) on a persistent grid, unless the segments
+// overflow one wave of resident teams by less than what `kh` (teams of LH
+// = half_team lanes) can hold at once: then the last segments would run as
+// a second wave behind their teams' first ones, so `kh` runs instead with
+// every segment resident from the start.
+template <typename K, typename KH, typename A>
+inline cudaError_t launch_one_wave(K k, int L, KH kh, int LH, A a, bool pdl, cudaStream_t s) {
+  const int64_t cap = resident_capacity(k);
+  if (LH < L) {
+    const int64_t cap_h = resident_capacity(kh);
+    if (a.nseg > cap * (256 / L) && a.nseg <= cap_h * (256 / LH)) {
+      a.lps = LH;
+      const int64_t need = (a.nseg * LH + 255) / 256;
+      return launch_ex(kh, need < cap_h ? need : cap_h, pdl, s, a);
+    }
+  }
+  a.lps = L;
+  const int64_t need = (a.nseg * L + 255) / 256;
+  return launch_ex(k, need < cap ? need : cap, pdl, s, a);
+}
+
 // CALL2(W, L) for the slice width and team size of a plan.
 #define SNACK_BW_LPS_SWITCH(bw, lps, CALL2)                                   \
   switch (bw * 64 + lps) {                                                    \

@@ -132,6 +132,29 @@ __device__ __forceinline__ void load_vec<1>(const float *p, float (&x)[1]) {
   x[0] = __ldg(p);
 }
 
+// Operand row slice: from global memory through the read-only path, or (SM)
+// from a copy in this block's shared memory.
+template <int VEC, bool SM>
+__device__ __forceinline__ void load_op(const float *p, float (&x)[VEC]) {
+  if constexpr (SM) {
+    if constexpr (VEC == 4) {
+      const float4 f = *reinterpret_cast<const float4 *>(p);
+      x[0] = f.x;
+      x[1] = f.y;
+      x[2] = f.z;
+      x[3] = f.w;
+    } else if constexpr (VEC == 2) {
+      const float2 f = *reinterpret_cast<const float2 *>(p);
+      x[0] = f.x;
+      x[1] = f.y;
+    } else {
+      x[0] = *p;
+    }
+  } else {
+    load_vec<VEC>(p, x);
+  }
+}
+
 // Lane (group 0, sub) holds batch b = v*G*VEC + sub*VEC + i.
 template <int BW>
 __device__ __forceinline__ void store_line(float *dst, int64_t ld, int nb, int line, int sub,
@@ -174,7 +197,7 @@ __device__ __forceinline__ void load_quad(const SpmmArgs &a, int kb, int k0, int
 
 // Gather the lane's slice of the dense rows of Q quads (all loads issued
 // before any use), then accumulate.
-template <int BW, int Q>
+template <int BW, int Q, bool SM = false>
 __device__ __forceinline__ void gather_fma(const float *src, const int (&c)[Q][4],
                                            const float (&w)[Q][4], const bool (&ok)[Q][4],
                                            float (&acc)[SliceShape<BW>::NV][SliceShape<BW>::VEC]) {
@@ -188,7 +211,7 @@ __device__ __forceinline__ void gather_fma(const float *src, const int (&c)[Q][4
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         if (ok[q][e]) {
-          load_vec<VEC>(src + (int64_t)c[q][e] * BW + v * G * VEC, x[q][e][v]);
+          load_op<VEC, SM>(src + (int64_t)c[q][e] * BW + v * G * VEC, x[q][e][v]);
         } else {
 #pragma unroll
           for (int i = 0; i < VEC; ++i) x[q][e][v][i] = 0.f;
@@ -210,8 +233,9 @@ __device__ __forceinline__ void gather_fma(const float *src, const int (&c)[Q][4
 // Segmented SpMM over blocks [block, ...) of a persistent grid of `nblocks`.
 // PERM = values reached through a column-order -> canonical permutation
 // (the dX = dY W direction).
-template <int BW, int LPS, bool PERM>
-__device__ __forceinline__ void spmm_part(const SpmmArgs &a, int64_t block, int64_t nblocks) {
+template <int BW, int LPS, bool PERM, bool SM = false>
+__device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, int64_t block,
+                                          int64_t nblocks) {
   using S = SliceShape<BW>;
   constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
   constexpr int lps = LPS;  // lanes per team: power of two in [G, 32]
@@ -225,7 +249,7 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, int64_t block, int6
   const int64_t stride = nblocks * teams_per_block;
   const int64_t my_team = block * teams_per_block + threadIdx.x / lps;
   const int64_t warp_team = block * teams_per_block + (threadIdx.x & ~31) / lps;
-  const float *src = a.src + sub * VEC;
+  const float *src = op + sub * VEC;
 
   for (int64_t t0 = 0; warp_team + t0 < a.nseg; t0 += stride) {
     const int64_t team = my_team + t0;
@@ -254,7 +278,7 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, int64_t block, int6
           const int k = kb + q * 4 * npt + e;
           ok[q][e] = k >= k0 && k < k1;
         }
-      gather_fma<BW, 2>(src, c, w, ok, acc);
+      gather_fma<BW, 2, SM>(src, c, w, ok, acc);
     }
     if (kb < k1) {
       int c[1][4];
@@ -263,7 +287,7 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, int64_t block, int6
       load_quad<PERM>(a, kb, k0, k1, c[0], w[0]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) ok[0][e] = kb + e >= k0 && kb + e < k1;
-      gather_fma<BW, 1>(src, c, w, ok, acc);
+      gather_fma<BW, 1, SM>(src, c, w, ok, acc);
     }
 
     // Combine the npt groups of the team (every lane of the warp is here).
@@ -320,7 +344,7 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, int64_t block, int6
 
 // dW for up to two quads of one group: the G lanes of a group each form part
 // of the batch dot product and meet by shuffle.
-template <int BW>
+template <int BW, bool SM>
 __device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt, int kb, int k0,
                                             int k1, int npt, unsigned gmask, int sub,
                                             const float (&dy)[SliceShape<BW>::NV]
@@ -348,7 +372,7 @@ __device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt,
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         if (ok) {
-          load_vec<VEC>(xt + (int64_t)c[q][e] * BW + v * G * VEC, x[q][e][v]);
+          load_op<VEC, SM>(xt + (int64_t)c[q][e] * BW + v * G * VEC, x[q][e][v]);
         } else {
 #pragma unroll
           for (int i = 0; i < VEC; ++i) x[q][e][v][i] = 0.f;
@@ -394,8 +418,9 @@ __device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt,
 
 // dW[k] = sum_b dY[b][row_k] X[b][col_k] over the row segments (persistent
 // grid of `nblocks`; a team's lanes stay together, groups never diverge).
-template <int BW, int LPS>
-__device__ __forceinline__ void sddmm_part(const SddmmArgs &a, int64_t block, int64_t nblocks) {
+template <int BW, int LPS, bool SM = false>
+__device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, int64_t block,
+                                           int64_t nblocks) {
   using S = SliceShape<BW>;
   constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
   constexpr int lps = LPS;
@@ -408,7 +433,7 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, int64_t block, in
   const unsigned gmask = G == 1 ? (1u << lane) : (((1u << G) - 1u) << (lane & ~(G - 1)));
   const int64_t teams_per_block = blockDim.x / lps;
   const int64_t stride = nblocks * teams_per_block;
-  const float *xt = a.xt + sub * VEC;
+  const float *xt = op + sub * VEC;
   for (int64_t team = block * teams_per_block + threadIdx.x / lps; team < a.nseg; team += stride) {
     const int4 sg = a.seg[team];
     const int r = sg.x, k0 = sg.y, k1 = sg.z;
@@ -420,8 +445,8 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, int64_t block, in
     }
     int kb = (k0 & ~3) + 4 * grp;
     for (; kb + 4 * npt < k1; kb += 8 * npt)
-      sddmm_quads<BW>(a, xt, kb, k0, k1, npt, gmask, sub, dy, true);
-    if (kb < k1) sddmm_quads<BW>(a, xt, kb, k0, k1, npt, gmask, sub, dy, false);
+      sddmm_quads<BW, SM>(a, xt, kb, k0, k1, npt, gmask, sub, dy, true);
+    if (kb < k1) sddmm_quads<BW, SM>(a, xt, kb, k0, k1, npt, gmask, sub, dy, false);
   }
 }
 
@@ -433,14 +458,14 @@ __global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
                     blockIdx.x, gridDim.x);
   if (PERM) prefetch_share(a.val, a.nval, blockIdx.x, gridDim.x);
   griddep_wait();
-  spmm_part<BW, LPS, PERM>(a, blockIdx.x, gridDim.x);
+  spmm_part<BW, LPS, PERM>(a, a.src, blockIdx.x, gridDim.x);
 }
 
 template <int BW, int LPS>
 __global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
   prefetch_segments(a.seg, a.nseg, a.col, nullptr, LPS, blockIdx.x, gridDim.x);
   griddep_wait();
-  sddmm_part<BW, LPS>(a, blockIdx.x, gridDim.x);
+  sddmm_part<BW, LPS>(a, a.xt, blockIdx.x, gridDim.x);
 }
 
 // Both backward products in one launch: the first `cols_blocks` blocks run
@@ -458,9 +483,9 @@ __global__ void __launch_bounds__(256) backward_segments(const SpmmArgs cols, co
   }
   griddep_wait();
   if ((int)blockIdx.x < cols_blocks)
-    spmm_part<BW, LPS, true>(cols, blockIdx.x, cols_blocks);
+    spmm_part<BW, LPS, true>(cols, cols.src, blockIdx.x, cols_blocks);
   else
-    sddmm_part<BW, LPS>(rows, blockIdx.x - cols_blocks, gridDim.x - cols_blocks);
+    sddmm_part<BW, LPS>(rows, rows.xt, blockIdx.x - cols_blocks, gridDim.x - cols_blocks);
 }
 
 // dst[c * BW + b] = b < nb ? src[b * ld + c] : 0 for 32 columns per block.
