@@ -9,10 +9,11 @@ batch).  Default workload: the GPT-2-small MLP projections 3072x768 and
 768x3072 at 95% sparsity, batch 1, 8 and 32.
 
 Timing: W warm-up steps, then K steps, each replayed from a CUDA graph of
-the step and timed with CUDA events on the launching stream; a 256 MiB
-buffer (about twice the L2) is written between steps so every step starts
-with a cold L2.  Barrier + synchronize on both sides; the max over ranks is
-reported.  Under torchrun every rank runs its own replica (weak scaling, no
+the step and timed with CUDA events on the launching stream; between steps
+a 256 MiB buffer (about twice the L2) is written and then read back, so
+every step starts with a cold L2 holding only clean lines (the flush's own
+write-backs are not charged to the step).  Barrier + synchronize on both
+sides; the max over ranks is reported.  Under torchrun every rank runs its own replica (weak scaling, no
 collective on the data path).
 
 Also reported: the roofline of the dominant op (metric bytes / measured
@@ -167,6 +168,15 @@ def metric_bytes(op: str, nnz: int, out: int, inp: int, B: int) -> int:
     return nnz * 12 + 4 * B * (inp + out)  # bwd_weight: X and dY read, dW in the 12
 
 
+def flush_l2(buf):
+    """Evict the workload from L2 before a timed step: write a buffer twice
+    the size of L2, then read it back.  The read pass writes the dirty lines
+    back to HBM and leaves L2 holding clean lines of the flush buffer, so the
+    timed step starts cold without paying for the flush's own write-backs."""
+    buf.fill_(1.0)
+    buf.sum()
+
+
 def read_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -264,7 +274,7 @@ def run_ours(args):
     wall0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for e0, e1 in evs:
-            flush.fill_(1.0)
+            flush_l2(flush)
             e0.record(stream)
             graph.replay()
             e1.record(stream)
@@ -302,7 +312,7 @@ def run_ours(args):
                     g_op.replay()
                     ts = []
                     for _ in range(reps):
-                        flush.fill_(1.0)
+                        flush_l2(flush)
                         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                         e0.record(stream)
                         g_op.replay()
@@ -357,7 +367,7 @@ def run_ours(args):
     barrier()
     with torch.cuda.stream(stream):
         for _ in range(args.steps):
-            flush.fill_(1.0)
+            flush_l2(flush)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             e2e_step()
@@ -385,7 +395,8 @@ def run_ours(args):
                 "batches": sorted({B for c in cases for B in c["acts"]}),
                 "ops_per_step": "fwd + fused bwd (dX, dW) per layer per batch",
                 "launch": "CUDA graph replay of the step",
-                "l2": "flushed between timed steps (256 MiB write); flush not timed",
+                "l2": "flushed between timed steps (256 MiB write, then read back); "
+                      "flush not timed",
                 "parallelism": f"{world} independent replica(s)"},
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -490,7 +501,7 @@ def run_only_op(args):
     dW = torch.empty(L.nnz, device="cuda")
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda")
     for _ in range(args.reps):
-        flush.fill_(1.0)
+        flush_l2(flush)
         if args.only_op == "fwd":
             sn.snack_forward(h, X, Y)
         elif args.only_op == "bwd_input":
