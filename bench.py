@@ -322,9 +322,12 @@ def run_ours(args):
                     del g_op
                     us = statistics.mean(a.elapsed_time(b) for a, b in ts) * 1e3
                     nbytes = metric_bytes(op, L.nnz, L.out, L.inp, B)
+                    bw, lanes, segs = sn.snack_plan(
+                        c["h"], ("fwd", "bwd_input", "bwd_weight").index(op), B)
                     ops.append(dict(op=op, layer=L.name, shape=f"{L.out}x{L.inp}", nnz=L.nnz, B=B,
                                     us=round(us, 3), gflops=round(2 * L.nnz * B / us / 1e3, 2),
-                                    gbs=round(nbytes / us / 1e3, 1), bytes=nbytes))
+                                    gbs=round(nbytes / us / 1e3, 1), bytes=nbytes,
+                                    plan=dict(slice=bw, lanes=lanes, segments=segs)))
     peak, peak_kind = read_peak()
     for o in ops:
         o["frac"] = round(o["gbs"] / peak, 4)

@@ -10,9 +10,11 @@
 //    dX = dY W) and each line is cut into segments.  A TEAM of LPS lanes
 //    owns one segment; inside a team, GROUPS of G lanes each take one entry
 //    at a time, and the G lanes of a group split the batch slice (BW floats,
-//    16-byte vectors).  Each group walks 4 consecutive entries per step from
-//    one 16-byte load of indices and one of values (aligned down to a
-//    multiple of 4 and masked at the segment ends), two such quads in flight.
+//    16-byte vectors).  Each group walks quads of 4 consecutive entries, each
+//    from one 16-byte load of indices and one of values (aligned down to a
+//    multiple of 4 and masked at the segment ends), two quads per step.
+//    Gathering from global memory in canonical order (forward, dW), the
+//    loads of the next step are issued before the gathers of this one.
 //  * The dense operand is gathered from a transposed copy (line-major,
 //    [lines][BW]) so that the BW batch values of one column are contiguous.
 //    A group reads an entry's whole row (up to one 128-byte line) with ONE
@@ -230,6 +232,66 @@ __device__ __forceinline__ void gather_fma(const float *src, const int (&c)[Q][4
           acc[v][i] = fmaf(ok[q][e] ? w[q][e] : 0.f, x[q][e][v][i], acc[v][i]);
 }
 
+// Index and value quads of one step (at kb and kb + 4 * npt, each only if
+// it starts inside the segment), canonical-order streams only.
+__device__ __forceinline__ void load_step(const SpmmArgs &a, int kb, int k1, int npt,
+                                          int (&c)[2][4], float (&w)[2][4]) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int kq = kb + q * 4 * npt;
+    if (kq >= k1) continue;
+    const int4 c4 = ld_stream_i4(a.idx + kq);
+    const float4 v4 = ld_stream_f4(a.val + kq);
+    c[q][0] = c4.x;
+    c[q][1] = c4.y;
+    c[q][2] = c4.z;
+    c[q][3] = c4.w;
+    w[q][0] = v4.x;
+    w[q][1] = v4.y;
+    w[q][2] = v4.z;
+    w[q][3] = v4.w;
+  }
+}
+
+// The entries of one group in steps of two quads, gathering the operand
+// from global memory, for canonical-order streams (rows).  The stream loads
+// run one step ahead: while this step's operand rows are gathered, the next
+// step's indices and values are in flight.  A quad past the segment end is
+// not loaded and all its entries are masked.  (The column direction reads
+// its values through the permutation, a load that depends on another; run
+// ahead the same way it measured slower at 64-wide slices, so it keeps the
+// plain loop.)
+template <int BW>
+__device__ __forceinline__ void walk_pipelined(const SpmmArgs &a, const float *src, int kb, int k0,
+                                               int k1, int npt,
+                                               float (&acc)[SliceShape<BW>::NV]
+                                                           [SliceShape<BW>::VEC]) {
+  int c[2][4] = {};
+  float w[2][4] = {};
+  load_step(a, kb, k1, npt, c, w);
+  for (; kb < k1; kb += 8 * npt) {
+    bool ok[2][4];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int k = kb + q * 4 * npt + e;
+        ok[q][e] = k >= k0 && k < k1;
+      }
+    int cn[2][4] = {};
+    float wn[2][4] = {};
+    load_step(a, kb + 8 * npt, k1, npt, cn, wn);
+    gather_fma<BW, 2, false>(src, c, w, ok, acc);
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        c[q][e] = cn[q][e];
+        w[q][e] = wn[q][e];
+      }
+  }
+}
+
 // Segmented SpMM over blocks [block, ...) of a persistent grid of `nblocks`.
 // PERM = values reached through a column-order -> canonical permutation
 // (the dX = dY W direction).
@@ -265,29 +327,33 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
       for (int i = 0; i < VEC; ++i) acc[v][i] = 0.f;
 
     int kb = (k0 & ~3) + 4 * grp;
-    for (; kb + 4 * npt < k1; kb += 8 * npt) {  // two quads in flight
-      int c[2][4];
-      float w[2][4];
-      bool ok[2][4];
-      load_quad<PERM>(a, kb, k0, k1, c[0], w[0]);
-      load_quad<PERM>(a, kb + 4 * npt, k0, k1, c[1], w[1]);
+    if constexpr (!SM && !PERM) {
+      walk_pipelined<BW>(a, src, kb, k0, k1, npt, acc);
+    } else {
+      for (; kb + 4 * npt < k1; kb += 8 * npt) {  // two quads in flight
+        int c[2][4];
+        float w[2][4];
+        bool ok[2][4];
+        load_quad<PERM>(a, kb, k0, k1, c[0], w[0]);
+        load_quad<PERM>(a, kb + 4 * npt, k0, k1, c[1], w[1]);
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k = kb + q * 4 * npt + e;
-          ok[q][e] = k >= k0 && k < k1;
-        }
-      gather_fma<BW, 2, SM>(src, c, w, ok, acc);
-    }
-    if (kb < k1) {
-      int c[1][4];
-      float w[1][4];
-      bool ok[1][4];
-      load_quad<PERM>(a, kb, k0, k1, c[0], w[0]);
+          for (int e = 0; e < 4; ++e) {
+            const int k = kb + q * 4 * npt + e;
+            ok[q][e] = k >= k0 && k < k1;
+          }
+        gather_fma<BW, 2, SM>(src, c, w, ok, acc);
+      }
+      if (kb < k1) {
+        int c[1][4];
+        float w[1][4];
+        bool ok[1][4];
+        load_quad<PERM>(a, kb, k0, k1, c[0], w[0]);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) ok[0][e] = kb + e >= k0 && kb + e < k1;
-      gather_fma<BW, 1, SM>(src, c, w, ok, acc);
+        for (int e = 0; e < 4; ++e) ok[0][e] = kb + e >= k0 && kb + e < k1;
+        gather_fma<BW, 1, SM>(src, c, w, ok, acc);
+      }
     }
 
     // Combine the npt groups of the team (every lane of the warp is here).
@@ -342,27 +408,32 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
   }
 }
 
-// dW for up to two quads of one group: the G lanes of a group each form part
-// of the batch dot product and meet by shuffle.
-template <int BW, bool SM>
-__device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt, int kb, int k0,
-                                            int k1, int npt, unsigned gmask, int sub,
-                                            const float (&dy)[SliceShape<BW>::NV]
-                                                             [SliceShape<BW>::VEC],
-                                            bool two) {
-  using S = SliceShape<BW>;
-  constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
-  int c[2][4];
-  float x[2][4][NV][VEC];
+// Column quads at kb and kb + 4 * npt, each only if it starts before k1.
+__device__ __forceinline__ void load_col_step(const int32_t *col, int kb, int k1, int npt,
+                                              int (&c)[2][4]) {
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
-    if (q == 1 && !two) break;
-    const int4 c4 = ld_stream_i4(a.col + kb + q * 4 * npt);
+    const int kq = kb + q * 4 * npt;
+    if (kq >= k1) continue;
+    const int4 c4 = ld_stream_i4(col + kq);
     c[q][0] = c4.x;
     c[q][1] = c4.y;
     c[q][2] = c4.z;
     c[q][3] = c4.w;
   }
+}
+
+// dW for up to two quads of one group (columns already loaded): the G lanes
+// of a group each form part of the batch dot product and meet by shuffle.
+template <int BW, bool SM>
+__device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt, int kb, int k0,
+                                            int k1, int npt, unsigned gmask, int sub,
+                                            const float (&dy)[SliceShape<BW>::NV]
+                                                             [SliceShape<BW>::VEC],
+                                            const int (&c)[2][4], bool two) {
+  using S = SliceShape<BW>;
+  constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
+  float x[2][4][NV][VEC];
 #pragma unroll
   for (int q = 0; q < 2; ++q)
 #pragma unroll
@@ -443,10 +514,25 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, 
 #pragma unroll
       for (int v = 0; v < NV; ++v) load_vec<VEC>(p + v * G * VEC, dy[v]);
     }
+    // Gathering from global memory, the column loads run one step ahead of
+    // the gathers (as in walk_pipelined); from shared memory they do not.
     int kb = (k0 & ~3) + 4 * grp;
-    for (; kb + 4 * npt < k1; kb += 8 * npt)
-      sddmm_quads<BW, SM>(a, xt, kb, k0, k1, npt, gmask, sub, dy, true);
-    if (kb < k1) sddmm_quads<BW, SM>(a, xt, kb, k0, k1, npt, gmask, sub, dy, false);
+    int c[2][4] = {};
+    if (!SM) load_col_step(a.col, kb, k1, npt, c);
+    for (; kb < k1; kb += 8 * npt) {
+      int cn[2][4] = {};
+      if (SM)
+        load_col_step(a.col, kb, k1, npt, c);
+      else
+        load_col_step(a.col, kb + 8 * npt, k1, npt, cn);
+      sddmm_quads<BW, SM>(a, xt, kb, k0, k1, npt, gmask, sub, dy, c, kb + 4 * npt < k1);
+      if (!SM) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) c[q][e] = cn[q][e];
+      }
+    }
   }
 }
 
