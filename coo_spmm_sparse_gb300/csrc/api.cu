@@ -110,7 +110,10 @@ snack::SpmmArgs spmm_args(snack::Layer &L, bool rows, const float *op, float *ds
 
 // Forward Y = X W^T over batch slices of at most 64: the slice of X is
 // transposed into the workspace (not needed for a single row), then the
-// row-segment kernel runs as a programmatic dependent of that transpose.
+// row-segment kernel runs.  Every launch is a programmatic dependent of the
+// kernel before it on the stream (the caller's or this call's own): its
+// launch and start-up overlap that kernel's end, and it waits for it before
+// touching memory.
 snack_status run_forward(snack_handle h, const float *X, float *Y, int64_t batch, cudaStream_t s) {
   snack::Layer &L = h->L;
   for (int64_t b0 = 0; b0 < batch; b0 += snack::kMaxSlice) {
@@ -119,15 +122,15 @@ snack_status run_forward(snack_handle h, const float *X, float *Y, int64_t batch
     const float *op = X + b0 * L.in;
     const bool transposed = p.bw > 1;
     if (transposed) {
-      cudaError_t e = snack::launch_transpose(op, L.in, nb, L.in, L.d_xt, p.bw, s);
+      cudaError_t e = snack::launch_transpose(op, L.in, nb, L.in, L.d_xt, p.bw, s, true);
       if (e != cudaSuccess) return cuda_fail(h, e, "transpose launch");
       g_launches.fetch_add(1, std::memory_order_relaxed);
       op = L.d_xt;
     }
     const snack::SpmmArgs a = spmm_args(L, true, op, Y + b0 * L.out, nb);
     cudaError_t e = snack::resident_fits(p.bw, L.in, L.csr.nseg)
-                        ? snack::launch_resident_spmm(false, p, a, L.in, L.d_err, transposed, s)
-                        : snack::launch_spmm_rows(p, a, transposed, s);
+                        ? snack::launch_resident_spmm(false, p, a, L.in, L.d_err, true, s)
+                        : snack::launch_spmm_rows(p, a, true, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "forward launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }
@@ -147,8 +150,8 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
   const bool transposed = pc.bw > 1;
   if (transposed) {
     cudaError_t e = dW ? snack::launch_transpose_pair(dyt, L.out, L.out, L.d_dyt, xt, L.in, L.in,
-                                                      L.d_xt, nb, pc.bw, s)
-                       : snack::launch_transpose(dyt, L.out, nb, L.out, L.d_dyt, pc.bw, s);
+                                                      L.d_xt, nb, pc.bw, s, true)
+                       : snack::launch_transpose(dyt, L.out, nb, L.out, L.d_dyt, pc.bw, s, true);
     if (e != cudaSuccess) return cuda_fail(h, e, "transpose launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
     dyt = L.d_dyt;
@@ -174,28 +177,26 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     // Operand resident in shared memory for at least one product (and, when
     // both are wanted, a layer large enough that a second launch is cheap):
     // one launch per product, the second waiting for the first.
-    bool pdl = transposed;
     if (dX) {
-      e = res_c ? snack::launch_resident_spmm(true, pc, cols, L.out, L.d_err, pdl, s)
-                : snack::launch_spmm_cols(pc, cols, pdl, s);
+      e = res_c ? snack::launch_resident_spmm(true, pc, cols, L.out, L.d_err, true, s)
+                : snack::launch_spmm_cols(pc, cols, true, s);
       if (e != cudaSuccess) return cuda_fail(h, e, "backward-input launch");
       g_launches.fetch_add(1, std::memory_order_relaxed);
-      pdl = true;
     }
     if (dW) {
-      e = res_r ? snack::launch_resident_sddmm(pr, rows, L.in, L.d_err, pdl, s)
-                : snack::launch_sddmm(pr, rows, pdl, s);
+      e = res_r ? snack::launch_resident_sddmm(pr, rows, L.in, L.d_err, true, s)
+                : snack::launch_sddmm(pr, rows, true, s);
       if (e != cudaSuccess) return cuda_fail(h, e, "backward-weight launch");
       g_launches.fetch_add(1, std::memory_order_relaxed);
     }
     return SNACK_OK;
   }
   if (dX && dW)
-    e = snack::launch_backward_fused(pc, cols, pr, rows, transposed, s);
+    e = snack::launch_backward_fused(pc, cols, pr, rows, true, s);
   else if (dX)
-    e = snack::launch_spmm_cols(pc, cols, transposed, s);
+    e = snack::launch_spmm_cols(pc, cols, true, s);
   else
-    e = snack::launch_sddmm(pr, rows, transposed, s);
+    e = snack::launch_sddmm(pr, rows, true, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "backward launch");
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return SNACK_OK;

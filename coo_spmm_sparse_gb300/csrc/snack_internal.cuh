@@ -113,7 +113,7 @@ int entry_lanes(int bw);
 
 // Launchers (spmm_*.cu).  Return the launch's cudaError_t.
 // pdl: launch as a programmatic dependent of the previous kernel on the
-// stream (only when that kernel is this call's own transpose).
+// stream (the kernels wait for it before touching any memory it may use).
 cudaError_t launch_spmm_rows(const Plan &p, const SpmmArgs &a, bool pdl, cudaStream_t s);
 cudaError_t launch_spmm_cols(const Plan &p, const SpmmArgs &a, bool pdl, cudaStream_t s);
 cudaError_t launch_sddmm(const Plan &p, const SddmmArgs &a, bool pdl, cudaStream_t s);
@@ -130,10 +130,10 @@ cudaError_t launch_resident_sddmm(const Plan &p, const SddmmArgs &a, int64_t n_o
 // at[c * bw + b] = a[b * a_ld + c] and bt likewise, in one launch.
 cudaError_t launch_transpose_pair(const float *a, int64_t a_ld, int64_t a_cols, float *at,
                                   const float *b, int64_t b_ld, int64_t b_cols, float *bt, int nb,
-                                  int bw, cudaStream_t s);
+                                  int bw, cudaStream_t s, bool pdl = false);
 // dst[c * bw + b] = b < nb ? src[b * ld + c] : 0, for c < ncols, b < bw.
 cudaError_t launch_transpose(const float *src, int64_t ld, int nb, int64_t ncols, float *dst,
-                             int bw, cudaStream_t s);
+                             int bw, cudaStream_t s, bool pdl = false);
 
 // Topology (topology.cu).
 snack_status build_topology(Layer &L, int64_t nnz, const int32_t *d_row_user,

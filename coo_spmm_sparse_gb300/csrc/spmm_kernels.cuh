@@ -92,6 +92,13 @@ __device__ __forceinline__ void prefetch_share(const float *p, int64_t n, int64_
 
 // Programmatic dependent launch: wait for the preceding grid (no-op when the
 // kernel was launched without the attribute) / let the next grid launch.
+// Every kernel here is launched as a programmatic dependent and waits before
+// it reads or writes anything a preceding kernel may touch (operands,
+// outputs, values, workspace), so only its launch, block start-up and the L2
+// prefetch of the handle's immutable index streams run ahead.  Transposes
+// trigger their dependents on entry; the segment kernels let theirs launch
+// when they finish (triggering on entry measured slower in a replayed step:
+// the early dependents hold block slots the running kernel could use).
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -538,8 +545,8 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, 
 
 template <int BW, int LPS, bool PERM>
 __global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
-  // Index / value streams do not depend on the transpose this kernel may
-  // follow: start pulling them into L2 before waiting for it.
+  // Index / value streams do not depend on the kernel this one may follow:
+  // start pulling them into L2 before waiting for it.
   prefetch_segments(a.seg, a.nseg, a.idx, PERM ? (const void *)a.perm : (const void *)a.val, LPS,
                     blockIdx.x, gridDim.x);
   if (PERM) prefetch_share(a.val, a.nval, blockIdx.x, gridDim.x);
@@ -598,6 +605,7 @@ __global__ void __launch_bounds__(256) transpose_pad(const float *__restrict__ s
                                                      float *__restrict__ dst) {
   __shared__ float buf[BW][33];
   griddep_launch();
+  griddep_wait();
   transpose_tile<BW>(src, ld, nb, ncols, dst, blockIdx.x, buf);
 }
 
@@ -611,6 +619,7 @@ __global__ void __launch_bounds__(256) transpose_pair(const float *__restrict__ 
                                                       int nb, int64_t a_tiles) {
   __shared__ float buf[BW][33];
   griddep_launch();
+  griddep_wait();
   if ((int64_t)blockIdx.x < a_tiles)
     transpose_tile<BW>(a, a_ld, nb, a_cols, at, blockIdx.x, buf);
   else
