@@ -10,6 +10,9 @@ CPU-baseline leg of ``bench.py`` do.  The arithmetic lives in
 * ``forward``             §3.1 Algorithm 1
 * ``backward_input``      §3.4, Appendix F (W^T by swapping index arrays)
 * ``backward_weight``     §3.4, Appendix F (sparse outer product, mini-batch)
+* ``weight_gradient64``   the same gradient left in float64
+* ``sgd_update``          §3.4 / §4.1 SGD on the stored entries (textbook rule)
+* ``adam_update``         Appendix G Adam on the stored entries (Kingma & Ba)
 * ``uniform_init``        §3.3 Algorithm 2 (getrand = counter SplitMix64)
 * ``prune_regrow``        Appendix G (magnitude prune, Algorithm 2 regrow)
 
@@ -78,6 +81,13 @@ def _load():
             fn.argtypes = [i64, i64, i64, p, p, p, i64, p, p, p]
             fn.restype = ctypes.c_int
         lib.oracle_backward_weight.argtypes = [i64, i64, i64, p, p, i64, p, p, p, p]
+        lib.oracle_weight_gradient64.argtypes = [i64, i64, i64, p, p, i64, p, p, p, p]
+        lib.oracle_weight_gradient64.restype = ctypes.c_int
+        d = ctypes.c_double
+        lib.oracle_sgd_update.argtypes = [i64, p, p, p, d, d, d, p, p]
+        lib.oracle_sgd_update.restype = ctypes.c_int
+        lib.oracle_adam_update.argtypes = [i64, p, p, p, p, d, d, d, d, d, i64, p, p, p]
+        lib.oracle_adam_update.restype = ctypes.c_int
         lib.oracle_backward_weight.restype = ctypes.c_int
         lib.oracle_splitmix64.argtypes = [u64, u64]
         lib.oracle_splitmix64.restype = u64
@@ -179,6 +189,61 @@ def backward_weight(out: int, inp: int, row, col, X, dY):
     if rc != OK:
         raise OracleError(rc)
     return dW, S
+
+
+def weight_gradient64(out: int, inp: int, row, col, X, dY):
+    """The weight gradient at stored entries in float64 (not rounded).
+    Returns (g, S)."""
+    lib = _load()
+    row, col = _c(row, np.int32), _c(col, np.int32)
+    X, dY = _c(X, np.float32), _c(dY, np.float32)
+    B = X.shape[0]
+    assert X.shape == (B, inp) and dY.shape == (B, out)
+    g = np.empty(row.size, np.float64)
+    S = np.empty(row.size, np.float64)
+    rc = lib.oracle_weight_gradient64(out, inp, row.size, _ptr(row), _ptr(col), B,
+                                      _ptr(X), _ptr(dY), _ptr(g), _ptr(S))
+    if rc != OK:
+        raise OracleError(rc)
+    return g, S
+
+
+def sgd_update(val, g, buf, lr: float, momentum: float = 0.0, weight_decay: float = 0.0):
+    """One SGD step on stored values (float32 val / buf in, float64 out).
+    Returns (val_new, buf_new); buf may be None when momentum == 0."""
+    lib = _load()
+    val = _c(val, np.float32)
+    g = _c(g, np.float64)
+    n = val.size
+    out = np.empty(n, np.float64)
+    if momentum != 0.0:
+        buf = _c(buf, np.float32)
+        bout = np.empty(n, np.float64)
+        bp, bo = _ptr(buf), _ptr(bout)
+    else:
+        bout, bp, bo = None, None, None
+    rc = lib.oracle_sgd_update(n, _ptr(val), _ptr(g), bp, lr, momentum, weight_decay,
+                               _ptr(out), bo)
+    if rc != OK:
+        raise OracleError(rc)
+    return out, bout
+
+
+def adam_update(val, g, m, v, lr: float, beta1: float, beta2: float, eps: float,
+                weight_decay: float, step: int):
+    """One Adam step on stored values (float32 val / m / v in, float64 out).
+    Returns (val_new, m_new, v_new)."""
+    lib = _load()
+    val = _c(val, np.float32)
+    g = _c(g, np.float64)
+    m, v = _c(m, np.float32), _c(v, np.float32)
+    n = val.size
+    out, mo, vo = (np.empty(n, np.float64) for _ in range(3))
+    rc = lib.oracle_adam_update(n, _ptr(val), _ptr(g), _ptr(m), _ptr(v), lr, beta1, beta2, eps,
+                                weight_decay, step, _ptr(out), _ptr(mo), _ptr(vo))
+    if rc != OK:
+        raise OracleError(rc)
+    return out, mo, vo
 
 
 def splitmix64(seed: int, t: int) -> int:

@@ -223,6 +223,86 @@ int oracle_backward_weight(int64_t out, int64_t in, int64_t nnz, const int32_t *
   return ORACLE_OK;
 }
 
+/*
+ * The same weight gradient left in double (no rounding to float), for the
+ * optimizer routines below: g[k] = sum over t of dY[t][row_k] * X[t][col_k].
+ */
+int oracle_weight_gradient64(int64_t out, int64_t in, int64_t nnz, const int32_t *row,
+                             const int32_t *col, int64_t B, const float *X, const float *dY,
+                             double *g, double *S) {
+  int64_t k, t;
+  for (k = 0; k < nnz; ++k) {
+    const int64_t i = row[k], j = col[k];
+    double acc = 0.0, sabs = 0.0;
+    for (t = 0; t < B; ++t) {
+      const double p = (double)dY[t * out + i] * (double)X[t * in + j];
+      acc += p;
+      sabs += fabs(p);
+    }
+    g[k] = acc;
+    if (S) S[k] = sabs;
+  }
+  return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Optimizer steps on the stored entries only                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * §3.4: the weight gradient exists only at supp(W), so the optimizer acts on
+ * the nnz stored values alone (frozen cells see no gradient and no update);
+ * §4.1 trains with SGD, Appendix G ("Optimization") with Adam.  The pages
+ * give neither update rule, so these are the textbook ones in the
+ * conventions of PyTorch's torch.optim.SGD and torch.optim.Adam, with L2
+ * weight decay added to the gradient.
+ *
+ * SGD, momentum mu >= 0 (no dampening, no Nesterov), one entry:
+ *   d = g + wd * w;  if mu > 0: buf = mu * buf + d, d = buf;  w = w - lr * d.
+ * With buf starting at 0 the first step gives buf = d, as PyTorch does.
+ * buf_in / buf_out may be NULL when mu == 0.
+ */
+int oracle_sgd_update(int64_t n, const float *val, const double *g, const float *buf_in,
+                      double lr, double mu, double wd, double *val_out, double *buf_out) {
+  int64_t k;
+  if (mu != 0.0 && (!buf_in || !buf_out)) return ORACLE_ERR_ARG;
+  for (k = 0; k < n; ++k) {
+    double d = g[k] + wd * (double)val[k];
+    if (mu != 0.0) {
+      d = mu * (double)buf_in[k] + d;
+      buf_out[k] = d;
+    }
+    val_out[k] = (double)val[k] - lr * d;
+  }
+  return ORACLE_OK;
+}
+
+/*
+ * Adam (Kingma and Ba, "Adam: A Method for Stochastic Optimization", ICLR
+ * 2015) with bias correction, step t >= 1, one entry:
+ *   d = g + wd * w
+ *   m = b1 * m + (1 - b1) * d
+ *   v = b2 * v + (1 - b2) * d^2
+ *   w = w - (lr / (1 - b1^t)) * m / (sqrt(v) / sqrt(1 - b2^t) + eps)
+ * (eps added after the bias-corrected square root, as in torch.optim.Adam).
+ */
+int oracle_adam_update(int64_t n, const float *val, const double *g, const float *m_in,
+                       const float *v_in, double lr, double b1, double b2, double eps, double wd,
+                       int64_t t, double *val_out, double *m_out, double *v_out) {
+  int64_t k;
+  if (t < 1) return ORACLE_ERR_ARG;
+  const double bc1 = 1.0 - pow(b1, (double)t), bc2 = 1.0 - pow(b2, (double)t);
+  for (k = 0; k < n; ++k) {
+    const double d = g[k] + wd * (double)val[k];
+    const double m = b1 * (double)m_in[k] + (1.0 - b1) * d;
+    const double v = b2 * (double)v_in[k] + (1.0 - b2) * d * d;
+    m_out[k] = m;
+    v_out[k] = v;
+    val_out[k] = (double)val[k] - (lr / bc1) * m / (sqrt(v) / sqrt(bc2) + eps);
+  }
+  return ORACLE_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* getrand(): a counter-based SplitMix64 stream                             */
 /* ------------------------------------------------------------------------ */

@@ -426,3 +426,89 @@ def test_nnz_rounding():
     assert workloads.nnz_for(8192, 8192, 99) == 671089      # 671088.64
     assert workloads.nnz_for(3072, 768, 95) == 117965       # 117964.8
     assert workloads.nnz_for(10000, 10000, 95) == 5_000_000
+
+
+# ------------------------------------------------------------ optimizer steps
+# The update rules are the textbook ones; torch.optim's CPU implementations
+# in float64 are the library routines they are pinned to, one step at a time
+# from a given (float32) state.
+
+def _torch_step(opt_cls, val, g, state, **kw):
+    import torch
+    p = torch.nn.Parameter(torch.from_numpy(np.asarray(val, np.float64).copy()))
+    opt = opt_cls([p], **kw)
+    if state:
+        opt.state[p] = state(p)
+    p.grad = torch.from_numpy(np.asarray(g, np.float64).copy())
+    opt.step()
+    return p.detach().numpy(), opt.state[p]
+
+
+def test_weight_gradient64_matches_rounded_gradient():
+    g = np.random.default_rng(40)
+    out, inp, B = 9, 7, 5
+    cells = g.choice(out * inp, 20, replace=False)
+    row, col = (cells // inp).astype(np.int32), (cells % inp).astype(np.int32)
+    X = g.standard_normal((B, inp)).astype(np.float32)
+    dY = g.standard_normal((B, out)).astype(np.float32)
+    g64, S = oracle.weight_gradient64(out, inp, row, col, X, dY)
+    dense = dY.astype(np.float64).T @ X.astype(np.float64)
+    assert np.allclose(g64, dense[row, col], rtol=1e-13, atol=1e-13)
+    dW, S2 = oracle.backward_weight(out, inp, row, col, X, dY)
+    assert np.array_equal(dW, g64.astype(np.float32)) and np.array_equal(S, S2)
+
+
+@pytest.mark.parametrize("momentum,wd", [(0.0, 0.0), (0.0, 0.01), (0.9, 0.0), (0.9, 5e-4)])
+def test_sgd_update_matches_torch(momentum, wd):
+    import torch
+    g = np.random.default_rng(41)
+    n = 50
+    val = g.standard_normal(n).astype(np.float32)
+    grad = g.standard_normal(n)
+    buf = g.standard_normal(n).astype(np.float32)
+    lr = 0.05
+    state = (lambda p: {"momentum_buffer": torch.from_numpy(buf.astype(np.float64))}) \
+        if momentum else None
+    want, st = _torch_step(torch.optim.SGD, val, grad, state, lr=lr, momentum=momentum,
+                           weight_decay=wd)
+    got, bout = oracle.sgd_update(val, grad, buf, lr, momentum, wd)
+    assert np.allclose(got, want, rtol=1e-14, atol=1e-15)
+    if momentum:
+        assert np.allclose(bout, st["momentum_buffer"].numpy(), rtol=1e-14, atol=1e-15)
+    # torch's first momentum step (no buffer yet) equals ours from a zero buffer
+    want0, _ = _torch_step(torch.optim.SGD, val, grad, None, lr=lr, momentum=momentum,
+                           weight_decay=wd)
+    got0, _ = oracle.sgd_update(val, grad, np.zeros(n, np.float32), lr, momentum, wd)
+    assert np.allclose(got0, want0, rtol=1e-14, atol=1e-15)
+
+
+@pytest.mark.parametrize("t,wd", [(1, 0.0), (2, 0.0), (7, 0.01), (1000, 0.0)])
+def test_adam_update_matches_torch(t, wd):
+    import torch
+    g = np.random.default_rng(42 + t)
+    n = 50
+    val = g.standard_normal(n).astype(np.float32)
+    grad = g.standard_normal(n) * 1e-2
+    m = (g.standard_normal(n) * 1e-2).astype(np.float32) if t > 1 else np.zeros(n, np.float32)
+    v = (g.random(n) * 1e-4).astype(np.float32) if t > 1 else np.zeros(n, np.float32)
+    kw = dict(lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=wd)
+
+    def state(p):
+        return {"step": torch.tensor(float(t - 1)),
+                "exp_avg": torch.from_numpy(m.astype(np.float64)),
+                "exp_avg_sq": torch.from_numpy(v.astype(np.float64))}
+    want, st = _torch_step(torch.optim.Adam, val, grad, state, **kw)
+    got, mo, vo = oracle.adam_update(val, grad, m, v, 1e-3, 0.9, 0.999, 1e-8, wd, t)
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-16)
+    assert np.allclose(mo, st["exp_avg"].numpy(), rtol=1e-13, atol=1e-20)
+    assert np.allclose(vo, st["exp_avg_sq"].numpy(), rtol=1e-13, atol=1e-24)
+
+
+def test_adam_first_step_closed_form():
+    # from zero moments the bias-corrected step is lr * g / (|g| + eps)
+    g = np.array([3.0, -0.25, 1e-9, 0.0])
+    val = np.array([1.0, 2.0, 3.0, 4.0], np.float32)
+    z = np.zeros(4, np.float32)
+    got, m, v = oracle.adam_update(val, g, z, z, 0.01, 0.9, 0.999, 1e-8, 0.0, 1)
+    assert np.allclose(got, val - 0.01 * g / (np.abs(g) + 1e-8), rtol=1e-15, atol=0)
+    assert np.allclose(m, 0.1 * g) and np.allclose(v, 0.001 * g * g)
