@@ -21,7 +21,8 @@ duration against the measured HBM copy bandwidth), an end-to-end number
 through the same calls with host buffers (pinned H2D of X and dY, D2H of Y,
 dX and dW inside the timed region), the CPU oracle on the host cores on a
 bounded sample, the SM clocks sampled during the timed region, and the
-kernel launches.
+kernel launches.  The per-op table also times the fused Adam step
+(snack_adam_step) of each layer and batch; it is not part of the metric.
 
 `--impl reference` times the CPU oracle instead (the deliberately slow
 reference arm), on the same workload and metric.
@@ -165,6 +166,8 @@ def metric_bytes(op: str, nnz: int, out: int, inp: int, B: int) -> int:
         return nnz * 12 + 4 * B * (inp + out)
     if op == "bwd_input":
         return nnz * 12 + 4 * B * (out + inp)
+    if op == "adam_step":  # column 4 B, value and two moments read and written 24 B
+        return nnz * 28 + 4 * B * (inp + out)
     return nnz * 12 + 4 * B * (inp + out)  # bwd_weight: X and dY read, dW in the 12
 
 
@@ -298,14 +301,19 @@ def run_ours(args):
             sn.snack_forward(c["h"], d["X"], d["Y"], stream=stream)
         elif op == "bwd_input":
             sn.snack_backward_input(c["h"], d["dY"], d["dX"], stream=stream)
-        else:
+        elif op == "bwd_weight":
             sn.snack_backward_weight(c["h"], d["X"], d["dY"], d["dW"], stream=stream)
+        else:  # fused Adam step (the gradient is not written); not part of the metric
+            sn.snack_adam_step(c["h"], d["X"], d["dY"], lr=1e-3, step=1, stream=stream)
 
     with torch.cuda.stream(stream):
         for c in cases:
             L = c["layer"]
             for B, d in c["dev"].items():
-                for op in ("fwd", "bwd_input", "bwd_weight"):
+                for op in ("fwd", "bwd_input", "bwd_weight", "adam_step"):
+                    if op == "adam_step":  # its first call allocates the moments
+                        run_op(op, c, d)
+                        torch.cuda.synchronize()
                     g_op = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(g_op, stream=stream):
                         run_op(op, c, d)
@@ -322,8 +330,8 @@ def run_ours(args):
                     del g_op
                     us = statistics.mean(a.elapsed_time(b) for a, b in ts) * 1e3
                     nbytes = metric_bytes(op, L.nnz, L.out, L.inp, B)
-                    bw, lanes, segs = sn.snack_plan(
-                        c["h"], ("fwd", "bwd_input", "bwd_weight").index(op), B)
+                    plan_op = {"fwd": 0, "bwd_input": 1}.get(op, 2)  # dW and Adam: rows
+                    bw, lanes, segs = sn.snack_plan(c["h"], plan_op, B)
                     ops.append(dict(op=op, layer=L.name, shape=f"{L.out}x{L.inp}", nnz=L.nnz, B=B,
                                     us=round(us, 3), gflops=round(2 * L.nnz * B / us / 1e3, 2),
                                     gbs=round(nbytes / us / 1e3, 1), bytes=nbytes,
@@ -331,7 +339,7 @@ def run_ours(args):
     peak, peak_kind = read_peak()
     for o in ops:
         o["frac"] = round(o["gbs"] / peak, 4)
-    dom = max(ops, key=lambda o: o["us"])
+    dom = max((o for o in ops if o["op"] != "adam_step"), key=lambda o: o["us"])
     tr = recorded_traffic(f"{dom['op']}:{dom['layer']}:B{dom['B']}", args.workload)
     roofline = {"bound": "hbm", "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": dom["frac"], "traffic": tr,
@@ -517,6 +525,43 @@ def run_only_op(args):
     print(f"only-op {args.only_op} {L.name} {L.out}x{L.inp} nnz={L.nnz} B={B} reps={args.reps}")
 
 
+def run_memory_sweep(args):
+    """Memory headroom (SNACK §4.4, Figure 4): device bytes of one sparse layer
+    against the dense W it replaces, at hidden size 10000 and input sizes
+    5000-25000, sparsity 90 / 95 / 99 %.  Prints one JSON object.
+
+    Per configuration: the handle's own accounting (snack_device_bytes:
+    indices, values, CSR/CSC layouts, segment tables, workspace), the device
+    memory the creation actually took (cudaMemGetInfo before / after, so
+    allocation granularity included), and the training-time total with the
+    nnz-long dW.  Dense references: W (4 B per cell), W + dW, and
+    Dense+Mask = W + dW + a 1-byte mask per cell."""
+    import torch
+    import coo_spmm_sparse_gb300 as sn
+    import workloads
+    torch.cuda.init()
+    hidden = 10000
+    rows = []
+    for inp in range(5000, 25001, 2500):
+        for sp in (90, 95, 99):
+            nnz = workloads.nnz_for(hidden, inp, sp)
+            torch.cuda.synchronize()
+            free0, _ = torch.cuda.mem_get_info()
+            h, _ = sn.snack_create_random(hidden, inp, nnz, args.seed)
+            torch.cuda.synchronize()
+            free1, _ = torch.cuda.mem_get_info()
+            acct = sn.snack_device_bytes(h)
+            cells = hidden * inp
+            rows.append(dict(inp=inp, hidden=hidden, sparsity=sp, nnz=nnz,
+                             snack_bytes=acct, snack_measured=free0 - free1,
+                             snack_train=acct + 4 * nnz,
+                             dense_w=4 * cells, dense_train=8 * cells,
+                             dense_mask_train=9 * cells))
+            del h
+    print(json.dumps({"metric": "device bytes of one layer vs dense", "hidden": hidden,
+                      "unit": "bytes", "rows": rows}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -533,11 +578,17 @@ def main(argv=None):
                     help="profiling mode: run one op --reps times on the first layer and "
                          "batch of the workload (cold L2 before each), print no JSON")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--memory-sweep", action="store_true",
+                    help="print the layer's device bytes against dense W at hidden 10000, "
+                         "input 5000-25000, sparsity 90/95/99 %% (one JSON object)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.only_op:
         run_only_op(args)
+        return
+    if args.memory_sweep:
+        run_memory_sweep(args)
         return
     if args.impl == "reference":
         run_reference(args)

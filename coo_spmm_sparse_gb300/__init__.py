@@ -32,7 +32,7 @@ _lib = _abi.load()
 __all__ = [
     "SnackError", "SnackHandle", "snack_create", "snack_create_random", "snack_forward",
     "snack_backward_input", "snack_backward_weight", "snack_backward", "snack_prune_regrow",
-    "snack_values", "snack_export", "snack_export_segments", "snack_plan", "snack_nnz",
+    "snack_values", "snack_sgd_step", "snack_adam_step", "snack_optimizer_state", "snack_export", "snack_export_segments", "snack_plan", "snack_nnz",
     "snack_device_bytes", "snack_destroy", "snack_launch_count", "snack_forward_csr_static", "snack_device_error", "SnackLinear", "library_path",
 ]
 
@@ -224,6 +224,41 @@ def snack_values(h: SnackHandle) -> torch.Tensor:
     if n == 0:
         return torch.empty(0, dtype=torch.float32, device=h.device)
     return torch.as_tensor(_CudaArray(p.value, n, h), device=h.device)
+
+
+def _opt_inputs(h: SnackHandle, X: torch.Tensor, dY: torch.Tensor):
+    X, dY = _dev_f32(X, "X"), _dev_f32(dY, "dY")
+    B = _batch(X, h.inp, "X")
+    if _batch(dY, h.out, "dY") != B:
+        raise ValueError("X and dY batch sizes differ")
+    return X, dY, B
+
+
+def snack_sgd_step(h: SnackHandle, X: torch.Tensor, dY: torch.Tensor, lr: float,
+                   momentum: float = 0.0, weight_decay: float = 0.0, stream=None) -> None:
+    """One SGD step on the stored values, fused with their gradient
+    sum_b dY[b,row_k] X[b,col_k] (which is not materialised)."""
+    X, dY, B = _opt_inputs(h, X, dY)
+    _check(_lib.snack_sgd_step(h.ptr, _ptr(X), _ptr(dY), B, lr, momentum, weight_decay,
+                               _stream(stream, X.device)), h)
+
+
+def snack_adam_step(h: SnackHandle, X: torch.Tensor, dY: torch.Tensor, lr: float = 1e-3,
+                    betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0,
+                    step: int = 1, stream=None) -> None:
+    """One Adam step (step = t >= 1) on the stored values, fused with their
+    gradient."""
+    X, dY, B = _opt_inputs(h, X, dY)
+    _check(_lib.snack_adam_step(h.ptr, _ptr(X), _ptr(dY), B, lr, betas[0], betas[1], eps,
+                                weight_decay, step, _stream(stream, X.device)), h)
+
+
+def snack_optimizer_state(h: SnackHandle, which: int) -> torch.Tensor:
+    """Optimizer state array `which` (0: momentum / first moment, 1: second
+    moment) as a CUDA tensor sharing the handle's memory (canonical order)."""
+    p = ctypes.c_void_p()
+    _check(_lib.snack_optimizer_state(h.ptr, which, ctypes.byref(p)), h)
+    return torch.as_tensor(_CudaArray(p.value, h.nnz, h), device=h.device)
 
 
 def snack_export(h: SnackHandle):

@@ -25,6 +25,9 @@ SIGNATURES = {
     "snack_backward_input": (ctypes.c_int, [vp, vp, vp, i64, vp]),
     "snack_backward_weight": (ctypes.c_int, [vp, vp, vp, vp, i64, vp]),
     "snack_backward": (ctypes.c_int, [vp, vp, vp, vp, vp, i64, vp]),
+    "snack_sgd_step": (ctypes.c_int, [vp, vp, vp, i64, f32, f32, f32, vp]),
+    "snack_adam_step": (ctypes.c_int, [vp, vp, vp, i64, f32, f32, f32, f32, f32, i64, vp]),
+    "snack_optimizer_state": (ctypes.c_int, [vp, ctypes.c_int, P(vp)]),
     "snack_prune_regrow": (ctypes.c_int, [vp, f32, u64, vp, P(i64), P(i64)]),
     "snack_values": (ctypes.c_int, [vp, P(vp)]),
     "snack_export": (ctypes.c_int, [vp, vp, vp, vp, ctypes.c_int, vp]),

@@ -2,6 +2,7 @@
 // Host-side orchestration only: argument checks, batch slicing, kernel
 // selection and launches.  All arithmetic runs in the kernels.
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -73,6 +74,9 @@ void account(snack::Layer &L) {
   b += (size_t)std::max(L.csr.nslots, L.csc.nslots) * snack::kMaxSlice * 4;
   b += (size_t)std::max(L.csr.nsplit, L.csc.nsplit) * 4;
   b += (size_t)(L.pan_csr.ncta + 1 + L.pan_csc.ncta + 1) * 4 + 4;  // panels, error flag
+  const float *extra[] = {L.d_opt[0], L.d_opt[1], L.d_gacc};  // optimizer state, gradient buffer
+  for (const float *p : extra)
+    if (p) b += (size_t)L.nnz_pad * 4;
   L.device_bytes = b;
 }
 
@@ -137,30 +141,37 @@ snack_status run_forward(snack_handle h, const float *X, float *Y, int64_t batch
   return SNACK_OK;
 }
 
-// One batch slice of the backward: dX (if dX) and / or dW (if dW).  One
-// launch transposes the slices of dY (and X when dW is wanted); one launch
-// then computes what is asked, both products sharing the transposed dY.
+// One batch slice of the backward: dX (if dX) and / or the weight product
+// (into dW, or, with an optimizer step in `opt`, into the values).  One
+// launch transposes the slices of dY (and X for the weight product); one
+// launch then computes what is asked, both products sharing the transposed
+// dY.
 snack_status run_backward_slice(snack_handle h, const float *X, const float *dY, float *dX,
-                                float *dW, int64_t b0, int nb, cudaStream_t s) {
+                                float *dW, int64_t b0, int nb, cudaStream_t s,
+                                const snack::OptArgs *opt = nullptr) {
   snack::Layer &L = h->L;
   const snack::Plan pc = snack::choose_plan(L.csc, nb);
   const snack::Plan pr = snack::choose_plan(L.csr, nb);
-  const float *xt = dW ? X + b0 * L.in : nullptr;
+  const bool fused_opt = opt && opt->kind != snack::kOptNone;
+  if (fused_opt && dX) return fail(h, SNACK_ERR_INVALID_ARG, "an optimizer step reads no dX");
+  const bool want_w = dW || fused_opt;  // the fused step writes values, not dW
+  const float *xt = want_w ? X + b0 * L.in : nullptr;
   const float *dyt = dY + b0 * L.out;
   const bool transposed = pc.bw > 1;
   if (transposed) {
-    cudaError_t e = dW ? snack::launch_transpose_pair(dyt, L.out, L.out, L.d_dyt, xt, L.in, L.in,
-                                                      L.d_xt, nb, pc.bw, s, true)
-                       : snack::launch_transpose(dyt, L.out, nb, L.out, L.d_dyt, pc.bw, s, true);
+    cudaError_t e =
+        want_w ? snack::launch_transpose_pair(dyt, L.out, L.out, L.d_dyt, xt, L.in, L.in, L.d_xt,
+                                              nb, pc.bw, s, true)
+               : snack::launch_transpose(dyt, L.out, nb, L.out, L.d_dyt, pc.bw, s, true);
     if (e != cudaSuccess) return cuda_fail(h, e, "transpose launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
     dyt = L.d_dyt;
-    if (dW) xt = L.d_xt;
+    if (want_w) xt = L.d_xt;
   }
   snack::SpmmArgs cols;
   if (dX) cols = spmm_args(L, false, dyt, dX + b0 * L.in, nb);
   snack::SddmmArgs rows;
-  if (dW) {
+  if (want_w) {
     rows.seg = L.csr.d_seg;
     rows.nseg = L.csr.nseg;
     rows.col = L.d_col;
@@ -169,11 +180,18 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     rows.dw = dW;
     rows.accumulate = b0 > 0;
     rows.lps = 32;
+    if (opt) rows.opt = *opt;
   }
   cudaError_t e;
   const bool res_c = dX && snack::resident_fits(pc.bw, L.out, L.csc.nseg);
-  const bool res_r = dW && snack::resident_fits(pr.bw, L.in, L.csr.nseg);
-  if ((res_c || res_r) && (!(dX && dW) || L.nnz >= (int64_t(1) << 19))) {
+  const bool res_r = want_w && !fused_opt && snack::resident_fits(pr.bw, L.in, L.csr.nseg);
+  if (fused_opt) {  // the optimizer step has its own kernel
+    e = snack::launch_sddmm_step(pr, rows, true, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "optimizer step launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return SNACK_OK;
+  }
+  if ((res_c || res_r) && (!(dX && want_w) || L.nnz >= (int64_t(1) << 19))) {
     // Operand resident in shared memory for at least one product (and, when
     // both are wanted, a layer large enough that a second launch is cheap):
     // one launch per product, the second waiting for the first.
@@ -183,7 +201,7 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
       if (e != cudaSuccess) return cuda_fail(h, e, "backward-input launch");
       g_launches.fetch_add(1, std::memory_order_relaxed);
     }
-    if (dW) {
+    if (want_w) {
       e = res_r ? snack::launch_resident_sddmm(pr, rows, L.in, L.d_err, true, s)
                 : snack::launch_sddmm(pr, rows, true, s);
       if (e != cudaSuccess) return cuda_fail(h, e, "backward-weight launch");
@@ -191,7 +209,7 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     }
     return SNACK_OK;
   }
-  if (dX && dW)
+  if (dX && want_w)
     e = snack::launch_backward_fused(pc, cols, pr, rows, true, s);
   else if (dX)
     e = snack::launch_spmm_cols(pc, cols, true, s);
@@ -201,6 +219,64 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return SNACK_OK;
 }
+
+// Optimizer state of the requested kind: allocated (zeroed) on first use;
+// state of another kind is zeroed first.
+snack_status ensure_opt_state(snack_handle h, int kind, int arrays, cudaStream_t s) {
+  snack::Layer &L = h->L;
+  cudaError_t e;
+  for (int i = 0; i < arrays; ++i) {
+    if (L.d_opt[i]) continue;
+    size_t acct = 0;
+    if ((e = snack::dev_alloc(&L.d_opt[i], (size_t)L.nnz_pad, &acct)) != cudaSuccess)
+      return cuda_fail(h, e, "optimizer state allocation");
+    if ((e = cudaMemsetAsync(L.d_opt[i], 0, (size_t)L.nnz_pad * 4, s)) != cudaSuccess)
+      return cuda_fail(h, e, "optimizer state zeroing");
+  }
+  if (L.opt_kind != kind) {
+    for (float *p : L.d_opt)
+      if (p && (e = cudaMemsetAsync(p, 0, (size_t)L.nnz_pad * 4, s)) != cudaSuccess)
+        return cuda_fail(h, e, "optimizer state zeroing");
+    L.opt_kind = kind;
+  }
+  account(L);
+  return SNACK_OK;
+}
+
+// The fused optimizer step over batch slices of at most 64: every slice but
+// the last adds its weight product into the handle's gradient buffer; the
+// last adds that buffer to its own product and applies the step.
+snack_status run_opt_step(snack_handle h, const float *X, const float *dY, int64_t batch,
+                          snack::OptArgs o, cudaStream_t s) {
+  snack::Layer &L = h->L;
+  if (L.nnz == 0) return SNACK_OK;
+  const bool sliced = batch > snack::kMaxSlice;
+  if (sliced && !L.d_gacc) {
+    size_t acct = 0;
+    cudaError_t e = snack::dev_alloc(&L.d_gacc, (size_t)L.nnz_pad, &acct);
+    if (e != cudaSuccess) return cuda_fail(h, e, "gradient buffer allocation");
+    account(L);
+  }
+  o.val = L.d_val;
+  o.s0 = L.d_opt[0];
+  o.s1 = o.kind == snack::kOptAdam ? L.d_opt[1] : nullptr;
+  if (o.kind == snack::kOptSgd && o.mom == 0.f) o.s0 = nullptr;
+  snack_status st;
+  for (int64_t b0 = 0; b0 < batch; b0 += snack::kMaxSlice) {
+    const int nb = (int)std::min<int64_t>(snack::kMaxSlice, batch - b0);
+    if (b0 + nb < batch) {
+      st = run_backward_slice(h, X, dY, nullptr, L.d_gacc, b0, nb, s);
+    } else {
+      snack::OptArgs last = o;
+      last.gacc = sliced ? L.d_gacc : nullptr;
+      st = run_backward_slice(h, X, dY, nullptr, nullptr, b0, nb, s, &last);
+    }
+    if (st != SNACK_OK) return st;
+  }
+  return SNACK_OK;
+}
+
+bool finite(float x) { return x == x && x - x == 0.f; }
 
 }  // namespace
 
@@ -369,6 +445,66 @@ snack_status snack_prune_regrow(snack_handle h, float prune_frac, uint64_t seed,
   account(h->L);
   if (n_pruned) *n_pruned = p;
   if (n_trials) *n_trials = t;
+  return SNACK_OK;
+}
+
+snack_status snack_sgd_step(snack_handle h, const float *X, const float *dY, int64_t batch,
+                            float lr, float momentum, float weight_decay, void *stream) {
+  if (!h) return fail(nullptr, SNACK_ERR_INVALID_ARG, "handle is NULL");
+  if (batch < 1) return fail(h, SNACK_ERR_INVALID_ARG, "batch must be >= 1");
+  if (!finite(lr) || !finite(momentum) || momentum < 0.f || !finite(weight_decay))
+    return fail(h, SNACK_ERR_INVALID_ARG, "lr and weight_decay must be finite, momentum >= 0");
+  snack_status st;
+  if ((st = check_dense(h, X, "X")) != SNACK_OK || (st = check_dense(h, dY, "dY")) != SNACK_OK ||
+      (st = check_device(h)) != SNACK_OK)
+    return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  snack::OptArgs o;
+  o.kind = snack::kOptSgd;
+  o.lr = lr;
+  o.mom = momentum;
+  o.wd = weight_decay;
+  if (momentum != 0.f && (st = ensure_opt_state(h, snack::kOptSgd, 1, s)) != SNACK_OK) return st;
+  return run_opt_step(h, X, dY, batch, o, s);
+}
+
+snack_status snack_adam_step(snack_handle h, const float *X, const float *dY, int64_t batch,
+                             float lr, float beta1, float beta2, float eps, float weight_decay,
+                             int64_t step, void *stream) {
+  if (!h) return fail(nullptr, SNACK_ERR_INVALID_ARG, "handle is NULL");
+  if (batch < 1) return fail(h, SNACK_ERR_INVALID_ARG, "batch must be >= 1");
+  if (step < 1) return fail(h, SNACK_ERR_INVALID_ARG, "step must be >= 1");
+  if (!finite(lr) || !finite(weight_decay) || !(beta1 >= 0.f && beta1 < 1.f) ||
+      !(beta2 >= 0.f && beta2 < 1.f) || !(eps > 0.f) || !finite(eps))
+    return fail(h, SNACK_ERR_INVALID_ARG,
+                "need finite lr, weight_decay; betas in [0, 1); finite eps > 0");
+  snack_status st;
+  if ((st = check_dense(h, X, "X")) != SNACK_OK || (st = check_dense(h, dY, "dY")) != SNACK_OK ||
+      (st = check_device(h)) != SNACK_OK)
+    return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = ensure_opt_state(h, snack::kOptAdam, 2, s)) != SNACK_OK) return st;
+  const double bc1 = 1.0 - std::pow((double)beta1, (double)step);
+  const double bc2 = 1.0 - std::pow((double)beta2, (double)step);
+  snack::OptArgs o;
+  o.kind = snack::kOptAdam;
+  o.wd = weight_decay;
+  o.b1 = beta1;
+  o.c1 = (float)(1.0 - (double)beta1);
+  o.b2 = beta2;
+  o.c2 = (float)(1.0 - (double)beta2);
+  o.eps = eps;
+  o.step = (float)((double)lr / bc1);
+  o.sbc2 = (float)std::sqrt(bc2);
+  return run_opt_step(h, X, dY, batch, o, s);
+}
+
+snack_status snack_optimizer_state(snack_handle h, int which, float **dev_state) {
+  if (!h || !dev_state) return fail(h, SNACK_ERR_INVALID_ARG, "NULL argument");
+  if (which < 0 || which > 1) return fail(h, SNACK_ERR_INVALID_ARG, "which must be 0 or 1");
+  if (!h->L.d_opt[which])
+    return fail(h, SNACK_ERR_INVALID_ARG, "no optimizer state of that index yet");
+  *dev_state = h->L.d_opt[which];
   return SNACK_OK;
 }
 

@@ -31,6 +31,7 @@
 namespace snack {
 
 constexpr int kMaxSlice = 64;  // widest batch slice one kernel launch handles
+constexpr int kOptNone = 0, kOptSgd = 1, kOptAdam = 2;  // fused optimizer kinds
 
 struct SegTable {
   int64_t nseg = 0;
@@ -69,6 +70,10 @@ struct Layer {
   float *d_dyt = nullptr;      // [out][64]  transposed dY slice
   float *d_partial = nullptr;  // [max(csr.nslots, csc.nslots)][64]
   int *d_counter = nullptr;    // [max(csr.nsplit, csc.nsplit)], zero between calls
+  // optimizer (allocated by the first fused step that needs them)
+  int opt_kind = kOptNone;     // kind the state below belongs to
+  float *d_opt[2] = {nullptr, nullptr};  // [nnz_pad] momentum / first moment, second moment
+  float *d_gacc = nullptr;     // [nnz_pad] gradient of earlier slices (batches above 64)
   size_t device_bytes = 0;
   std::string last_error;
 };
@@ -91,6 +96,20 @@ struct SpmmArgs {
   int64_t nval;         // floats in the padded value array (L2 prefetch bound)
 };
 
+// Optimizer step fused into the SDDMM epilogue (kind != kOptNone): the
+// gradient of each stored entry updates its value and state in place and
+// dW is not written.  Coefficients are prepared on the host.
+struct OptArgs {
+  int kind = kOptNone;
+  float lr = 0.f, mom = 0.f, wd = 0.f;            // SGD: lr, momentum; both: weight decay
+  float b1 = 0.f, c1 = 0.f, b2 = 0.f, c2 = 0.f;   // Adam: beta1, 1 - beta1, beta2, 1 - beta2
+  float eps = 0.f, step = 0.f, sbc2 = 1.f;        // Adam: eps, lr / (1 - b1^t), sqrt(1 - b2^t)
+  float *val = nullptr;                           // [nnz] values, canonical order
+  float *s0 = nullptr;                            // momentum buffer / first moment (or null)
+  float *s1 = nullptr;                            // second moment (Adam)
+  const float *gacc = nullptr;                    // gradient of earlier batch slices (or null)
+};
+
 struct SddmmArgs {
   const int4 *seg;
   int64_t nseg;
@@ -100,6 +119,7 @@ struct SddmmArgs {
   float *dw;         // [nnz]
   int accumulate;    // add to dw instead of overwriting (batch slices > 0)
   int lps;           // lanes per segment team (set by the launcher)
+  OptArgs opt;       // fused optimizer step instead of writing dw
 };
 
 // Kernel selection: batch slice width, lanes per entry group, lanes per segment.
@@ -117,6 +137,8 @@ int entry_lanes(int bw);
 cudaError_t launch_spmm_rows(const Plan &p, const SpmmArgs &a, bool pdl, cudaStream_t s);
 cudaError_t launch_spmm_cols(const Plan &p, const SpmmArgs &a, bool pdl, cudaStream_t s);
 cudaError_t launch_sddmm(const Plan &p, const SddmmArgs &a, bool pdl, cudaStream_t s);
+// The same with the optimizer step of a.opt applied instead of writing dW.
+cudaError_t launch_sddmm_step(const Plan &p, const SddmmArgs &a, bool pdl, cudaStream_t s);
 cudaError_t launch_backward_fused(const Plan &pc, const SpmmArgs &cols, const Plan &pr,
                                   const SddmmArgs &rows, bool pdl, cudaStream_t s);
 // Variants with the whole operand resident in shared memory (slices of 1-4

@@ -415,11 +415,97 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
   }
 }
 
-// Column quads at kb and kb + 4 * npt, each only if it starts before k1.
+// Four consecutive floats at p (16-byte aligned): one vector access when the
+// whole quad is in use, else only the entries whose bit is set in `mask`.
+__device__ __forceinline__ void load4(const float *p, unsigned mask, float (&x)[4]) {
+  if (mask == 15u) {
+    const float4 f = *reinterpret_cast<const float4 *>(p);
+    x[0] = f.x;
+    x[1] = f.y;
+    x[2] = f.z;
+    x[3] = f.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = (mask >> e) & 1u ? p[e] : 0.f;
+  }
+}
+
+__device__ __forceinline__ void store4(float *p, unsigned mask, const float (&x)[4]) {
+  if (mask == 15u) {
+    *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if ((mask >> e) & 1u) p[e] = x[e];
+  }
+}
+
+// Operands of the optimizer step for one quad (entries whose bit is set in
+// mask): values, state, and the gradient of earlier batch slices.  Loaded
+// before the quad's gathers so that their latency overlaps them.
+struct OptQuad {
+  unsigned mask;
+  float w[4], s0[4], s1[4], ga[4];
+};
+
+__device__ __forceinline__ unsigned quad_mask(int kq, int k0, int k1) {
+  unsigned mask = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (kq + e >= k0 && kq + e < k1) mask |= 1u << e;
+  return mask;
+}
+
+__device__ __forceinline__ void opt_load(const OptArgs &o, int kq, unsigned mask, OptQuad &q) {
+  q.mask = mask;
+  load4(o.val + kq, mask, q.w);
+  if (o.s0) load4(o.s0 + kq, mask, q.s0);
+  if (o.s1) load4(o.s1 + kq, mask, q.s1);
+  if (o.gacc) {
+    load4(o.gacc + kq, mask, q.ga);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) q.ga[e] = 0.f;
+  }
+}
+
+// Optimizer step for one quad given this batch slice's gradients res (plus
+// earlier slices' in q.ga).  SGD: d = g + wd w, buf = mom buf + d (with a
+// buffer), w -= lr d.  Adam: m = b1 m + (1-b1) d, v = b2 v + (1-b2) d^2,
+// w -= step m / (sqrt(v) / sqrt(1 - b2^t) + eps).
+__device__ __forceinline__ void opt_store(const OptArgs &o, int kq, OptQuad &q,
+                                          const float (&res)[4]) {
+  float d[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) d[e] = fmaf(o.wd, q.w[e], res[e] + q.ga[e]);
+  if (o.kind == kOptSgd) {
+    if (o.s0) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d[e] = q.s0[e] = fmaf(o.mom, q.s0[e], d[e]);
+      store4(o.s0 + kq, q.mask, q.s0);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) q.w[e] = fmaf(-o.lr, d[e], q.w[e]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      q.s0[e] = fmaf(o.b1, q.s0[e], o.c1 * d[e]);
+      q.s1[e] = fmaf(o.b2, q.s1[e], o.c2 * d[e] * d[e]);
+      q.w[e] = q.w[e] - o.step * q.s0[e] / (sqrtf(q.s1[e]) / o.sbc2 + o.eps);
+    }
+    store4(o.s0 + kq, q.mask, q.s0);
+    store4(o.s1 + kq, q.mask, q.s1);
+  }
+  store4(o.val + kq, q.mask, q.w);
+}
+
+// Column quads at kb (and kb + 4 * npt when QPS = 2), each only if it
+// starts before k1.
+template <int QPS>
 __device__ __forceinline__ void load_col_step(const int32_t *col, int kb, int k1, int npt,
                                               int (&c)[2][4]) {
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
+  for (int q = 0; q < QPS; ++q) {
     const int kq = kb + q * 4 * npt;
     if (kq >= k1) continue;
     const int4 c4 = ld_stream_i4(col + kq);
@@ -432,7 +518,7 @@ __device__ __forceinline__ void load_col_step(const int32_t *col, int kb, int k1
 
 // dW for up to two quads of one group (columns already loaded): the G lanes
 // of a group each form part of the batch dot product and meet by shuffle.
-template <int BW, bool SM>
+template <int BW, bool SM, bool OPT>
 __device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt, int kb, int k0,
                                             int k1, int npt, unsigned gmask, int sub,
                                             const float (&dy)[SliceShape<BW>::NV]
@@ -440,6 +526,16 @@ __device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt,
                                             const int (&c)[2][4], bool two) {
   using S = SliceShape<BW>;
   constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
+  OptQuad oq[OPT ? 2 : 1];
+  if constexpr (OPT) {
+    if (sub == 0) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int kq = kb + q * 4 * npt;
+        opt_load(a.opt, kq, (q == 0 || two) ? quad_mask(kq, k0, k1) : 0u, oq[q]);
+      }
+    }
+  }
   float x[2][4][NV][VEC];
 #pragma unroll
   for (int q = 0; q < 2; ++q)
@@ -474,6 +570,10 @@ __device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt,
       res[e] = s;
     }
     if (sub == 0) {
+      if constexpr (OPT) {
+        opt_store(a.opt, kq, oq[q], res);
+        continue;
+      }
       float *d = a.dw + kq;
       if (kq >= k0 && kq + 3 < k1) {
         float4 o = make_float4(res[0], res[1], res[2], res[3]);
@@ -496,7 +596,9 @@ __device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt,
 
 // dW[k] = sum_b dY[b][row_k] X[b][col_k] over the row segments (persistent
 // grid of `nblocks`; a team's lanes stay together, groups never diverge).
-template <int BW, int LPS, bool SM = false>
+// OPT: apply the optimizer step of a.opt instead of writing dW (compiled
+// separately, so the plain kernels keep their registers).
+template <int BW, int LPS, bool SM = false, bool OPT = false>
 __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, int64_t block,
                                            int64_t nblocks) {
   using S = SliceShape<BW>;
@@ -523,16 +625,20 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, 
     }
     // Gathering from global memory, the column loads run one step ahead of
     // the gathers (as in walk_pipelined); from shared memory they do not.
+    // Two quads per step, one with the optimizer step (its operands take the
+    // registers of the second quad).
+    constexpr int QPS = OPT ? 1 : 2;
     int kb = (k0 & ~3) + 4 * grp;
     int c[2][4] = {};
-    if (!SM) load_col_step(a.col, kb, k1, npt, c);
-    for (; kb < k1; kb += 8 * npt) {
+    if (!SM) load_col_step<QPS>(a.col, kb, k1, npt, c);
+    for (; kb < k1; kb += 4 * QPS * npt) {
       int cn[2][4] = {};
       if (SM)
-        load_col_step(a.col, kb, k1, npt, c);
+        load_col_step<QPS>(a.col, kb, k1, npt, c);
       else
-        load_col_step(a.col, kb + 8 * npt, k1, npt, cn);
-      sddmm_quads<BW, SM>(a, xt, kb, k0, k1, npt, gmask, sub, dy, c, kb + 4 * npt < k1);
+        load_col_step<QPS>(a.col, kb + 4 * QPS * npt, k1, npt, cn);
+      sddmm_quads<BW, SM, OPT>(a, xt, kb, k0, k1, npt, gmask, sub, dy, c,
+                               QPS == 2 && kb + 4 * npt < k1);
       if (!SM) {
 #pragma unroll
         for (int q = 0; q < 2; ++q)
@@ -554,11 +660,11 @@ __global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
   spmm_part<BW, LPS, PERM>(a, a.src, blockIdx.x, gridDim.x);
 }
 
-template <int BW, int LPS>
+template <int BW, int LPS, bool OPT = false>
 __global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
   prefetch_segments(a.seg, a.nseg, a.col, nullptr, LPS, blockIdx.x, gridDim.x);
   griddep_wait();
-  sddmm_part<BW, LPS>(a, a.xt, blockIdx.x, gridDim.x);
+  sddmm_part<BW, LPS, false, OPT>(a, a.xt, blockIdx.x, gridDim.x);
 }
 
 // Both backward products in one launch: the first `cols_blocks` blocks run

@@ -651,6 +651,14 @@ __global__ void regrown_values(const uint64_t *key, const uint32_t *src, int64_t
   val[k] = src[k] == kRegrown ? 0.f : old_val[src[k]];
 }
 
+// Per-entry optimizer state follows its entry through the new order; regrown
+// entries start from zero state.
+__global__ void carry_state(const uint32_t *src, int64_t n, const float *old, float *state) {
+  const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= n) return;
+  state[k] = src[k] == kRegrown ? 0.f : old[src[k]];
+}
+
 }  // namespace
 
 // ------------------------------------------------------------- public -----
@@ -782,6 +790,12 @@ snack_status prune_regrow(Layer &L, float frac, uint64_t seed, int64_t *pruned, 
   regrown_values<<<grid_for(n, 256), 256, 0, s>>>(k1, v1, n, L.in, old_val, L.d_row, L.d_col,
                                                   L.d_val);
   TRY_CUDA(cudaGetLastError());
+  for (float *state : L.d_opt) {
+    if (!state) continue;
+    TRY_CUDA(cudaMemcpyAsync(old_val, state, n * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    carry_state<<<grid_for(n, 256), 256, 0, s>>>(v1, n, old_val, state);
+    TRY_CUDA(cudaGetLastError());
+  }
   TRY_CUDA(cudaStreamSynchronize(s));
   return finish_layout(L, k1, s, err);
 }
@@ -790,7 +804,8 @@ void free_layer(Layer &L) {
   void *ptrs[] = {L.d_col,     L.d_row,     L.d_val,         L.d_row_ptr,     L.d_csc_row,
                   L.d_csc_perm, L.d_col_ptr, L.csr.d_seg,     L.csr.d_split,   L.csc.d_seg,
                   L.csc.d_split, L.d_xt,     L.d_dyt,         L.d_partial,     L.d_counter,
-                  L.pan_csr.d_ptr, L.pan_csc.d_ptr, L.d_err};
+                  L.pan_csr.d_ptr, L.pan_csc.d_ptr, L.d_err,   L.d_opt[0],      L.d_opt[1],
+                  L.d_gacc};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   L = Layer();

@@ -128,6 +128,50 @@ snack_status snack_backward(snack_handle h, const float *X, const float *dY, flo
                             float *dW, int64_t batch, void *stream);
 
 /*
+ * One optimizer step on the stored entries, fused with the weight gradient.
+ * §3.4: the gradient exists only at supp(W), so only the nnz stored values
+ * are trained (frozen cells see no gradient); §4.1 trains with SGD and
+ * Appendix G with Adam.  For every stored entry k, with
+ *   g_k = sum_{b<batch} dY[b][row_k] * X[b][col_k] + weight_decay * val_k
+ * (X, dY as for snack_backward_weight; dW is never written):
+ *   snack_sgd_step:  momentum > 0:  buf_k = momentum * buf_k + g_k,
+ *                                   val_k -= lr * buf_k
+ *                    momentum == 0: val_k -= lr * g_k   (no state)
+ *   snack_adam_step (Kingma and Ba, ICLR 2015; step = t >= 1):
+ *                    m_k = beta1 m_k + (1 - beta1) g_k
+ *                    v_k = beta2 v_k + (1 - beta2) g_k^2
+ *                    val_k -= lr / (1 - beta1^t) * m_k
+ *                             / (sqrt(v_k) / sqrt(1 - beta2^t) + eps)
+ * (the conventions of torch.optim.SGD without dampening and torch.optim.Adam).
+ * Values change in place: compute dX (snack_backward_input, which reads
+ * them) before the step.
+ *
+ * State: nnz-long fp32 arrays owned by the handle, in canonical order
+ * (snack_optimizer_state).  The first step that needs them allocates and
+ * zeroes them (that call allocates device memory, so make it outside graph
+ * capture); a step of the other optimizer kind zeroes them first.  Batches
+ * above 64 also use an nnz-long gradient buffer, allocated on first use.
+ * snack_prune_regrow keeps each surviving entry's state and starts regrown
+ * entries from zero.  Errors: SNACK_ERR_INVALID_ARG for non-finite lr /
+ * weight_decay, momentum < 0, betas outside [0, 1), eps <= 0, step < 1,
+ * batch < 1 or misaligned X / dY.  Asynchronous on `stream`.
+ */
+snack_status snack_sgd_step(snack_handle h, const float *X, const float *dY, int64_t batch,
+                            float lr, float momentum, float weight_decay, void *stream);
+snack_status snack_adam_step(snack_handle h, const float *X, const float *dY, int64_t batch,
+                             float lr, float beta1, float beta2, float eps, float weight_decay,
+                             int64_t step, void *stream);
+
+/*
+ * Device pointer to optimizer state array `which` (nnz floats, canonical
+ * order, owned by the handle): 0 = SGD momentum buffer or Adam first moment,
+ * 1 = Adam second moment.  SNACK_ERR_INVALID_ARG when that array does not
+ * exist yet.  The caller may read or overwrite it (e.g. to checkpoint and
+ * restore); the pointer stays valid until snack_destroy.
+ */
+snack_status snack_optimizer_state(snack_handle h, int which, float **dev_state);
+
+/*
  * One topology update (Appendix G "Sparsity schedule and DST"):
  *  1. prune P = floor((double)prune_frac * nnz) stored entries with the
  *     smallest |val|: ordered by the bit pattern of |val| as an unsigned
