@@ -284,13 +284,14 @@ def snack_export_segments(h: SnackHandle):
     return res
 
 
-def snack_plan(h: SnackHandle, op: int, batch: int, with_tiles: bool = False):
-    """(slice_width, lanes_per_segment, segments[, tile_cols]) chosen for op
-    0/1/2 at this batch; tile_cols = 0 means the segmented kernel runs."""
+def snack_plan(h: SnackHandle, op: int, batch: int, with_resident: bool = False):
+    """(slice_width, lanes_per_segment, segments[, resident]) chosen for op
+    0/1/2 at this batch; resident = 1 when every block holds the whole dense
+    operand in shared memory."""
     w, l, s, t = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int32()
     _check(_lib.snack_plan(h.ptr, op, batch, ctypes.byref(w), ctypes.byref(l), ctypes.byref(s),
                            ctypes.byref(t)), h)
-    if with_tiles:
+    if with_resident:
         return int(w.value), int(l.value), int(s.value), int(t.value)
     return int(w.value), int(l.value), int(s.value)
 

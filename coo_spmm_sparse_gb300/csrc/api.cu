@@ -243,14 +243,18 @@ snack_status ensure_opt_state(snack_handle h, int kind, int arrays, cudaStream_t
   return SNACK_OK;
 }
 
-// The fused optimizer step over batch slices of at most 64: every slice but
-// the last adds its weight product into the handle's gradient buffer; the
-// last adds that buffer to its own product and applies the step.
+// The fused optimizer step over batch slices of at most 64 (wider slices
+// measured slower: one lane of a group of 16 or 32 carries the update):
+// every slice but the last adds its weight product into the handle's
+// gradient buffer; the last adds that buffer to its own product and applies
+// the step.
+constexpr int64_t kStepSlice = 64;
+
 snack_status run_opt_step(snack_handle h, const float *X, const float *dY, int64_t batch,
                           snack::OptArgs o, cudaStream_t s) {
   snack::Layer &L = h->L;
   if (L.nnz == 0) return SNACK_OK;
-  const bool sliced = batch > snack::kMaxSlice;
+  const bool sliced = batch > kStepSlice;
   if (sliced && !L.d_gacc) {
     size_t acct = 0;
     cudaError_t e = snack::dev_alloc(&L.d_gacc, (size_t)L.nnz_pad, &acct);
@@ -262,8 +266,8 @@ snack_status run_opt_step(snack_handle h, const float *X, const float *dY, int64
   o.s1 = o.kind == snack::kOptAdam ? L.d_opt[1] : nullptr;
   if (o.kind == snack::kOptSgd && o.mom == 0.f) o.s0 = nullptr;
   snack_status st;
-  for (int64_t b0 = 0; b0 < batch; b0 += snack::kMaxSlice) {
-    const int nb = (int)std::min<int64_t>(snack::kMaxSlice, batch - b0);
+  for (int64_t b0 = 0; b0 < batch; b0 += kStepSlice) {
+    const int nb = (int)std::min<int64_t>(kStepSlice, batch - b0);
     if (b0 + nb < batch) {
       st = run_backward_slice(h, X, dY, nullptr, L.d_gacc, b0, nb, s);
     } else {
@@ -551,7 +555,7 @@ snack_status snack_export_segments(snack_handle h, int32_t *row_ptr, int32_t *co
 }
 
 snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_width,
-                        int32_t *lanes_per_segment, int64_t *segments, int32_t *tile_cols) {
+                        int32_t *lanes_per_segment, int64_t *segments, int32_t *resident) {
   if (!h) return fail(nullptr, SNACK_ERR_INVALID_ARG, "handle is NULL");
   if (op < 0 || op > 2 || batch < 1) return fail(h, SNACK_ERR_INVALID_ARG, "bad op or batch");
   const snack::SegTable &t = op == 1 ? h->L.csc : h->L.csr;
@@ -559,7 +563,8 @@ snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_wi
   if (slice_width) *slice_width = p.bw;
   if (lanes_per_segment) *lanes_per_segment = p.lanes;
   if (segments) *segments = t.nseg;
-  if (tile_cols) *tile_cols = 0;  // every op runs the segmented kernels
+  if (resident)
+    *resident = snack::resident_fits(p.bw, op == 1 ? h->L.out : h->L.in, t.nseg) ? 1 : 0;
   return SNACK_OK;
 }
 

@@ -18,7 +18,7 @@ cudaError_t launch_transpose(const float *src, int64_t ld, int nb, int64_t ncols
                              int bw, cudaStream_t s, bool pdl) {
   const int64_t tiles = (ncols + 31) / 32;
 #define SNACK_CALL(W) return launch_ex(transpose_pad<W>, tiles, pdl, s, src, ld, nb, ncols, dst);
-  SNACK_BW_SWITCH(bw, SNACK_CALL)
+  SNACK_BW_SWITCH_WIDE(bw, SNACK_CALL)
 #undef SNACK_CALL
 }
 
@@ -29,7 +29,7 @@ cudaError_t launch_transpose_pair(const float *a, int64_t a_ld, int64_t a_cols, 
 #define SNACK_CALL(W)                                                                    \
   return launch_ex(transpose_pair<W>, a_tiles + b_tiles, pdl, s, a, a_ld, a_cols, at, b, \
                    b_ld, b_cols, bt, nb, a_tiles);
-  SNACK_BW_SWITCH(bw, SNACK_CALL)
+  SNACK_BW_SWITCH_WIDE(bw, SNACK_CALL)
 #undef SNACK_CALL
 }
 

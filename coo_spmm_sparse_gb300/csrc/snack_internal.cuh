@@ -30,7 +30,7 @@
 
 namespace snack {
 
-constexpr int kMaxSlice = 64;  // widest batch slice one kernel launch handles
+constexpr int kMaxSlice = 256;  // widest batch slice one kernel launch handles
 constexpr int kOptNone = 0, kOptSgd = 1, kOptAdam = 2;  // fused optimizer kinds
 
 struct SegTable {
@@ -66,9 +66,9 @@ struct Layer {
   int32_t *d_col_ptr = nullptr;
   SegTable csr, csc;
   // workspace
-  float *d_xt = nullptr;       // [in][64]   transposed X slice
-  float *d_dyt = nullptr;      // [out][64]  transposed dY slice
-  float *d_partial = nullptr;  // [max(csr.nslots, csc.nslots)][64]
+  float *d_xt = nullptr;       // [in][kMaxSlice]   transposed X slice
+  float *d_dyt = nullptr;      // [out][kMaxSlice]  transposed dY slice
+  float *d_partial = nullptr;  // [max(csr.nslots, csc.nslots)][kMaxSlice]
   int *d_counter = nullptr;    // [max(csr.nsplit, csc.nsplit)], zero between calls
   // optimizer (allocated by the first fused step that needs them)
   int opt_kind = kOptNone;     // kind the state below belongs to

@@ -85,6 +85,15 @@ inline int team_lanes(const Plan &p) {
       return cudaErrorInvalidValue; \
   }
 
+// The same with the wide slices of the handle path (128, 256).
+#define SNACK_BW_SWITCH_WIDE(bw, CALL) \
+  switch (bw) {                        \
+    case 128: CALL(128)                \
+    case 256: CALL(256)                \
+    default:                           \
+      SNACK_BW_SWITCH(bw, CALL)        \
+  }
+
 // Team size one step down from L for slice width W (L itself if none).
 constexpr int half_team(int W, int L) {
   return (L / 2 >= 8 && L / 2 >= lanes_for(W)) ? L / 2 : L;
@@ -124,7 +133,8 @@ inline cudaError_t launch_one_wave(K k, int L, KH kh, int LH, A a, bool pdl, cud
     case 16 * 64 + 32: CALL2(16, 32) case 32 * 64 + 8: CALL2(32, 8)           \
     case 32 * 64 + 16: CALL2(32, 16) case 32 * 64 + 32: CALL2(32, 32)         \
     case 64 * 64 + 8: CALL2(64, 8) case 64 * 64 + 16: CALL2(64, 16)           \
-    case 64 * 64 + 32: CALL2(64, 32)                                          \
+    case 64 * 64 + 32: CALL2(64, 32) case 128 * 64 + 16: CALL2(128, 16)       \
+    case 128 * 64 + 32: CALL2(128, 32) case 256 * 64 + 32: CALL2(256, 32)     \
     default:                                                                  \
       return cudaErrorInvalidValue;                                           \
   }

@@ -105,8 +105,11 @@ __device__ __forceinline__ void griddep_launch() {
 }
 
 // Lanes per entry for a slice width: one 16-byte vector per lane and the
-// whole row (up to 128 B) in one instruction; BW = 64 uses 8 lanes x 2.
-__host__ __device__ constexpr int lanes_for(int bw) { return bw <= 4 ? 1 : (bw >= 32 ? 8 : bw / 4); }
+// whole row (up to 128 B) in one instruction; BW = 64 uses 8 lanes x 2, the
+// wide slices (128, 256) a half or whole warp x 2.
+__host__ __device__ constexpr int lanes_for(int bw) {
+  return bw <= 4 ? 1 : (bw >= 128 ? bw / 8 : (bw >= 32 ? 8 : bw / 4));
+}
 
 // Shape of a batch slice: each lane holds NV vectors of VEC floats.
 template <int BW>
@@ -610,7 +613,8 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, 
   const int tlane = lane & (lps - 1);
   const int grp = tlane / G;
   const int sub = tlane % G;
-  const unsigned gmask = G == 1 ? (1u << lane) : (((1u << G) - 1u) << (lane & ~(G - 1)));
+  const unsigned gmask = G == 32 ? 0xffffffffu
+                                 : (G == 1 ? (1u << lane) : (((1u << G) - 1u) << (lane & ~(G - 1))));
   const int64_t teams_per_block = blockDim.x / lps;
   const int64_t stride = nblocks * teams_per_block;
   const float *xt = op + sub * VEC;

@@ -30,6 +30,7 @@ constexpr int64_t kStaticScratchFloats = int64_t(1) << 21;
 __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
 
 constexpr int kMaxDevices = 64;
+constexpr int kStaticSlice = 64;  // widest batch slice this entry point runs
 std::mutex g_scratch_mu;
 float *g_scratch_addr[kMaxDevices] = {};
 
@@ -166,7 +167,7 @@ extern "C" snack_status snack_forward_csr_static(int64_t out_features, int64_t i
       (nnz > 0 && (!aligned(col, 16) || !aligned(val, 16))))
     return fail(SNACK_ERR_INVALID_ARG,
                 "col, val, X and Y must be 16-byte aligned, row_ptr 4-byte aligned");
-  const int first_width = slice_width(batch < kMaxSlice ? batch : kMaxSlice);
+  const int first_width = slice_width(batch < kStaticSlice ? batch : kStaticSlice);
   if (first_width > 1 && in_features * first_width > kStaticScratchFloats)
     return fail(SNACK_ERR_UNSUPPORTED,
                 "in_features x batch slice width (" + std::to_string(in_features) + " x " +
@@ -193,8 +194,8 @@ extern "C" snack_status snack_forward_csr_static(int64_t out_features, int64_t i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   SegTable shape;
   shape.mean_len = (double)nnz / (double)out_features;
-  for (int64_t b0 = 0; b0 < batch; b0 += kMaxSlice) {
-    const int nb = (int)((batch - b0) < kMaxSlice ? (batch - b0) : kMaxSlice);
+  for (int64_t b0 = 0; b0 < batch; b0 += kStaticSlice) {
+    const int nb = (int)((batch - b0) < kStaticSlice ? (batch - b0) : kStaticSlice);
     const Plan p = choose_plan(shape, nb);
     const float *op = X + b0 * in_features;
     if (p.bw > 1) {

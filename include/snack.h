@@ -35,7 +35,8 @@
  *     the handle as it was.
  *   - Limits: 1 <= out_features, in_features < 2^31; 0 <= nnz < 2^31 and
  *     nnz <= out_features * in_features; batch >= 1 (any size: batches above
- *     64 run as consecutive slices of 64).
+ *     256 run as consecutive slices of 256; the fused optimizer steps use
+ *     slices of 64).
  */
 #ifndef SNACK_H
 #define SNACK_H
@@ -218,13 +219,15 @@ snack_status snack_export_segments(snack_handle h, int32_t *row_ptr, int32_t *co
 /*
  * Which kernel variant a call would run: for op 0 = forward, 1 =
  * backward_input, 2 = backward_weight and the given batch, returns the
- * batch slice width (1, 2, 4, 8, 16, 32 or 64), the lanes that share one
- * row (or column) segment, the number of segments, and the operand lines per
- * shared-memory tile of the panel x tile kernel (0 when the segmented kernel
- * runs instead).  Any output may be NULL.  Pure host query.
+ * batch slice width (1, 2, 4, 8, 16, 32, 64, 128 or 256), the lanes that
+ * share one row (or column) segment (the launch may halve them when that
+ * keeps every segment in one wave of resident teams), the number of
+ * segments, and whether every block holds the whole dense operand in shared
+ * memory (1) or gathers it from global memory (0).  Any output may be NULL.
+ * Pure host query.
  */
 snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_width,
-                        int32_t *lanes_per_segment, int64_t *segments, int32_t *tile_cols);
+                        int32_t *lanes_per_segment, int64_t *segments, int32_t *resident);
 
 /*
  * Forward pass Y = X W^T for callers that cannot allocate device memory.

@@ -112,7 +112,7 @@ def _uniform_case(out, inp, sparsity, seed):
     return Case(out, inp, row, col, val, seed + 1)
 
 
-@pytest.mark.parametrize("B", [1, 4, 16, 130])
+@pytest.mark.parametrize("B", [1, 4, 16, 130, 300])
 def test_sgd_plain_and_momentum(B):
     c = _uniform_case(256, 256, 90, 30)
     c.sgd(B, 0.05, 0.0, 0.0)
@@ -123,7 +123,8 @@ def test_sgd_plain_and_momentum(B):
 
 @pytest.mark.parametrize("shape,B", [((256, 256, 90), 4), ((3072, 768, 95), 1),
                                      ((3072, 768, 95), 8), ((768, 3072, 95), 32),
-                                     ((3000, 3000, 85), 64), ((700, 900, 80), 130)])
+                                     ((3000, 3000, 85), 64), ((700, 900, 80), 130),
+                                     ((700, 900, 80), 300)])
 def test_adam_steps(shape, B):
     c = _uniform_case(*shape, 31)
     for t in (1, 2, 3):

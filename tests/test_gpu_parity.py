@@ -20,7 +20,7 @@ from parity_util import (assert_close, canonical, check_products, check_topology
 
 pytestmark = pytest.mark.gpu
 
-ALL_B = [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 130]
+ALL_B = [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 130, 256, 300]
 
 
 def _layer_case(out, inp, row, col, val, batches, seed=0, fused=True):
@@ -151,7 +151,7 @@ def test_dense_lines_full_oracle():
     ref = canonical(out, inp, row, col, val)
     h = sn().snack_create(out, inp, row, col, val)
     g = np.random.default_rng(12)
-    for B in (4, 8, 16, 33, 64, 70):
+    for B in (4, 8, 16, 33, 64, 70, 200, 260):
         X = g.standard_normal((B, inp)).astype(np.float32)
         dY = g.standard_normal((B, out)).astype(np.float32)
         check_products(h, out, inp, ref, X, dY)
@@ -300,9 +300,15 @@ def test_invalid_inputs_return_status():
 def test_plan_follows_batch_and_row_length():
     L = workloads.workload("large99").layers[0]
     h, _ = sn().snack_create_random(L.out, L.inp, L.nnz, 1)
-    for B, w in ((1, 1), (2, 2), (3, 4), (5, 8), (16, 16), (17, 32), (64, 64), (300, 64)):
+    for B, w in ((1, 1), (2, 2), (3, 4), (5, 8), (16, 16), (17, 32), (64, 64), (65, 128),
+                 (129, 256), (300, 256)):
         assert sn().snack_plan(h, 0, B)[0] == w
     assert sn().snack_plan(h, 0, 16)[1] == 32            # 100 entries per row
+    # the whole 10000-line operand (40-160 KB) is staged in shared memory up
+    # to 4-wide slices; wider slices gather from global memory
+    assert sn().snack_plan(h, 0, 1, with_resident=True)[3] == 1
+    assert sn().snack_plan(h, 1, 4, with_resident=True)[3] == 1
+    assert sn().snack_plan(h, 0, 16, with_resident=True)[3] == 0
     small = workloads.workload("toy256").layers[0]
     r, c, v = small.coo()
     h2 = sn().snack_create(small.out, small.inp, r, c, v)
