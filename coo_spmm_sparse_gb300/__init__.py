@@ -32,7 +32,7 @@ _lib = _abi.load()
 __all__ = [
     "SnackError", "SnackHandle", "snack_create", "snack_create_random", "snack_forward",
     "snack_backward_input", "snack_backward_weight", "snack_backward", "snack_prune_regrow",
-    "snack_values", "snack_sgd_step", "snack_adam_step", "snack_optimizer_state", "snack_export", "snack_export_segments", "snack_plan", "snack_nnz",
+    "snack_values", "snack_values_changed", "snack_sgd_step", "snack_adam_step", "snack_optimizer_state", "snack_export", "snack_export_segments", "snack_plan", "snack_nnz",
     "snack_device_bytes", "snack_destroy", "snack_launch_count", "snack_forward_csr_static", "snack_device_error", "SnackLinear", "library_path",
 ]
 
@@ -224,6 +224,12 @@ def snack_values(h: SnackHandle) -> torch.Tensor:
     if n == 0:
         return torch.empty(0, dtype=torch.float32, device=h.device)
     return torch.as_tensor(_CudaArray(p.value, n, h), device=h.device)
+
+
+def snack_values_changed(h: SnackHandle, stream=None) -> None:
+    """Declare that writes through the snack_values() view are done: the
+    handle re-derives its column-ordered value copy and dX streams it again."""
+    _check(_lib.snack_values_changed(h.ptr, _stream(stream, h.device)), h)
 
 
 def _opt_inputs(h: SnackHandle, X: torch.Tensor, dY: torch.Tensor):

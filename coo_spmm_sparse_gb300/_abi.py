@@ -30,6 +30,7 @@ SIGNATURES = {
     "snack_optimizer_state": (ctypes.c_int, [vp, ctypes.c_int, P(vp)]),
     "snack_prune_regrow": (ctypes.c_int, [vp, f32, u64, vp, P(i64), P(i64)]),
     "snack_values": (ctypes.c_int, [vp, P(vp)]),
+    "snack_values_changed": (ctypes.c_int, [vp, vp]),
     "snack_export": (ctypes.c_int, [vp, vp, vp, vp, ctypes.c_int, vp]),
     "snack_export_segments": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
     "snack_plan": (ctypes.c_int, [vp, ctypes.c_int, i64, P(i32), P(i32), P(i64), P(i32)]),

@@ -74,8 +74,9 @@ void account(snack::Layer &L) {
   b += (size_t)std::max(L.csr.nslots, L.csc.nslots) * snack::kMaxSlice * 4;
   b += (size_t)std::max(L.csr.nsplit, L.csc.nsplit) * 4;
   b += (size_t)(L.pan_csr.ncta + 1 + L.pan_csc.ncta + 1) * 4 + 4;  // panels, error flag
-  const float *extra[] = {L.d_opt[0], L.d_opt[1], L.d_gacc};  // optimizer state, gradient buffer
-  for (const float *p : extra)
+  // column-ordered values; optimizer state, gradient buffer, copy positions
+  const void *extra[] = {L.d_val_csc, L.d_opt[0], L.d_opt[1], L.d_gacc, L.d_csc_pos};
+  for (const void *p : extra)
     if (p) b += (size_t)L.nnz_pad * 4;
   L.device_bytes = b;
 }
@@ -101,6 +102,10 @@ snack::SpmmArgs spmm_args(snack::Layer &L, bool rows, const float *op, float *ds
   a.idx = rows ? L.d_col : L.d_csc_row;
   a.val = L.d_val;
   a.perm = rows ? nullptr : L.d_csc_perm;
+  if (!rows && L.csc_vals) {  // values already in column order: no permutation
+    a.val = L.d_val_csc;
+    a.perm = nullptr;
+  }
   a.src = op;
   a.dst = dst;
   a.ld = rows ? L.out : L.in;
@@ -139,6 +144,12 @@ snack_status run_forward(snack_handle h, const float *X, float *Y, int64_t batch
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }
   return SNACK_OK;
+}
+
+// dX over the column segments: through the permutation, or (values in
+// column order) with the canonical-order kernels.
+cudaError_t launch_cols(const snack::Plan &p, const snack::SpmmArgs &a, cudaStream_t s) {
+  return a.perm ? snack::launch_spmm_cols(p, a, true, s) : snack::launch_spmm_rows(p, a, true, s);
 }
 
 // One batch slice of the backward: dX (if dX) and / or the weight product
@@ -196,8 +207,9 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     // both are wanted, a layer large enough that a second launch is cheap):
     // one launch per product, the second waiting for the first.
     if (dX) {
-      e = res_c ? snack::launch_resident_spmm(true, pc, cols, L.out, L.d_err, true, s)
-                : snack::launch_spmm_cols(pc, cols, true, s);
+      e = res_c ? snack::launch_resident_spmm(cols.perm != nullptr, pc, cols, L.out, L.d_err,
+                                              true, s)
+                : launch_cols(pc, cols, s);
       if (e != cudaSuccess) return cuda_fail(h, e, "backward-input launch");
       g_launches.fetch_add(1, std::memory_order_relaxed);
     }
@@ -212,7 +224,7 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
   if (dX && want_w)
     e = snack::launch_backward_fused(pc, cols, pr, rows, true, s);
   else if (dX)
-    e = snack::launch_spmm_cols(pc, cols, true, s);
+    e = launch_cols(pc, cols, s);
   else
     e = snack::launch_sddmm(pr, rows, true, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "backward launch");
@@ -265,6 +277,16 @@ snack_status run_opt_step(snack_handle h, const float *X, const float *dY, int64
   o.s0 = L.d_opt[0];
   o.s1 = o.kind == snack::kOptAdam ? L.d_opt[1] : nullptr;
   if (o.kind == snack::kOptSgd && o.mom == 0.f) o.s0 = nullptr;
+  if (L.csc_vals) {  // keep the column-ordered copy of the values current
+    if (!L.d_csc_pos) {
+      std::string err;
+      snack_status st = snack::build_csc_pos(L, s, err);
+      if (st != SNACK_OK) return fail(h, st, err);
+      account(L);
+    }
+    o.val_csc = L.d_val_csc;
+    o.csc_pos = L.d_csc_pos;
+  }
   snack_status st;
   for (int64_t b0 = 0; b0 < batch; b0 += kStepSlice) {
     const int nb = (int)std::min<int64_t>(kStepSlice, batch - b0);
@@ -515,6 +537,21 @@ snack_status snack_optimizer_state(snack_handle h, int which, float **dev_state)
 snack_status snack_values(snack_handle h, float **dev_val) {
   if (!h || !dev_val) return fail(h, SNACK_ERR_INVALID_ARG, "NULL argument");
   *dev_val = h->L.d_val;
+  // The caller may write the values from now on: the column-ordered copy
+  // can no longer be trusted.
+  h->L.values_shared = true;
+  h->L.csc_vals = false;
+  return SNACK_OK;
+}
+
+snack_status snack_values_changed(snack_handle h, void *stream) {
+  if (!h) return fail(nullptr, SNACK_ERR_INVALID_ARG, "handle is NULL");
+  snack_status st = check_device(h);
+  if (st != SNACK_OK) return st;
+  h->L.values_shared = false;
+  std::string err;
+  if ((st = snack::refresh_csc_values(h->L, static_cast<cudaStream_t>(stream), err)) != SNACK_OK)
+    return fail(h, st, err);
   return SNACK_OK;
 }
 

@@ -18,7 +18,8 @@ cudaError_t launch_backward_fused(const Plan &pc, const SpmmArgs &cols_in, const
   if (need_c + need_r == 0) return cudaSuccess;
 #define SNACK_CALL(W, L)                                                            \
   {                                                                                 \
-    auto k = backward_segments<W, L>;                                               \
+    auto k = cols.perm ? backward_segments<W, L, true>                             \
+                       : backward_segments<W, L, false>;                           \
     const int64_t cap = resident_capacity(k);                                       \
     int64_t gc = need_c, gr = need_r;                                               \
     if (gc + gr > cap) {                                                            \

@@ -304,8 +304,10 @@ __device__ __forceinline__ void walk_pipelined(const SpmmArgs &a, const float *s
 
 // Segmented SpMM over blocks [block, ...) of a persistent grid of `nblocks`.
 // PERM = values reached through a column-order -> canonical permutation
-// (the dX = dY W direction).
-template <int BW, int LPS, bool PERM, bool SM = false>
+// (the dX = dY W direction while the column-ordered value copy is stale).
+// PIPE = with global gathers and no permutation, run the stream one step
+// ahead (walk_pipelined).
+template <int BW, int LPS, bool PERM, bool SM = false, bool PIPE = true>
 __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, int64_t block,
                                           int64_t nblocks) {
   using S = SliceShape<BW>;
@@ -337,7 +339,7 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
       for (int i = 0; i < VEC; ++i) acc[v][i] = 0.f;
 
     int kb = (k0 & ~3) + 4 * grp;
-    if constexpr (!SM && !PERM) {
+    if constexpr (!SM && !PERM && PIPE) {
       walk_pipelined<BW>(a, src, kb, k0, k1, npt, acc);
     } else {
       for (; kb + 4 * npt < k1; kb += 8 * npt) {  // two quads in flight
@@ -500,6 +502,11 @@ __device__ __forceinline__ void opt_store(const OptArgs &o, int kq, OptQuad &q,
     store4(o.s1 + kq, q.mask, q.s1);
   }
   store4(o.val + kq, q.mask, q.w);
+  if (o.val_csc) {  // the column-ordered copy: scattered, fire-and-forget stores
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if ((q.mask >> e) & 1u) o.val_csc[o.csc_pos[kq + e]] = q.w[e];
+  }
 }
 
 // Column quads at kb (and kb + 4 * npt when QPS = 2), each only if it
@@ -673,20 +680,25 @@ __global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
 
 // Both backward products in one launch: the first `cols_blocks` blocks run
 // dX over the column segments, the rest run dW over the row segments (one
-// team size for both parts).
-template <int BW, int LPS>
+// team size for both parts).  PERM: dX reads the values through the
+// column permutation (else from the column-ordered copy).  dX keeps the
+// plain loop here: the look-ahead's registers would cost the shared grid a
+// resident block per SM.
+template <int BW, int LPS, bool PERM>
 __global__ void __launch_bounds__(256) backward_segments(const SpmmArgs cols, const SddmmArgs rows,
                                                          int cols_blocks) {
   if ((int)blockIdx.x < cols_blocks) {
-    prefetch_segments(cols.seg, cols.nseg, cols.idx, cols.perm, LPS, blockIdx.x, cols_blocks);
-    prefetch_share(cols.val, cols.nval, blockIdx.x, cols_blocks);
+    prefetch_segments(cols.seg, cols.nseg, cols.idx,
+                      PERM ? (const void *)cols.perm : (const void *)cols.val, LPS, blockIdx.x,
+                      cols_blocks);
+    if (PERM) prefetch_share(cols.val, cols.nval, blockIdx.x, cols_blocks);
   } else {
     prefetch_segments(rows.seg, rows.nseg, rows.col, nullptr, LPS, blockIdx.x - cols_blocks,
                       gridDim.x - cols_blocks);
   }
   griddep_wait();
   if ((int)blockIdx.x < cols_blocks)
-    spmm_part<BW, LPS, true>(cols, cols.src, blockIdx.x, cols_blocks);
+    spmm_part<BW, LPS, PERM, false, false>(cols, cols.src, blockIdx.x, cols_blocks);
   else
     sddmm_part<BW, LPS>(rows, rows.xt, blockIdx.x - cols_blocks, gridDim.x - cols_blocks);
 }

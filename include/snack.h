@@ -88,7 +88,8 @@ snack_status snack_create(int64_t out_features, int64_t in_features, int64_t nnz
  * draw t of the counter-based SplitMix64 stream started at `seed` (the
  * finaliser applied to seed + (t+1) * 0x9E3779B97F4A7C15); a candidate
  * already drawn is rejected.  Values start at 0 (write them through
- * snack_values()).  n_trials (may be NULL) receives the number of
+ * snack_values(), then call snack_values_changed()).  n_trials (may be
+ * NULL) receives the number of
  * candidates drawn.  Synchronises `stream`.
  */
 snack_status snack_create_random(int64_t out_features, int64_t in_features, int64_t nnz,
@@ -196,8 +197,25 @@ snack_status snack_prune_regrow(snack_handle h, float prune_frac, uint64_t seed,
  * Device pointer to the nnz stored values in canonical order.  The caller
  * may read and write them in place (e.g. an optimizer step); they stay
  * valid until snack_destroy().
+ *
+ * The handle also keeps the values in column order, so that dX streams them
+ * instead of reading each through the column permutation.  Handing out this
+ * writable pointer makes that copy untrusted: from this call on, dX reads
+ * the values through the permutation (same results, slower) until
+ * snack_values_changed() is called.
  */
 snack_status snack_values(snack_handle h, float **dev_val);
+
+/*
+ * Tell the handle that the caller has finished writing the values through
+ * the snack_values() pointer: re-derives the column-ordered copy
+ * (asynchronous on `stream`) and lets dX use it again.  The library then
+ * assumes the values change only through its own calls (snack_sgd_step,
+ * snack_adam_step, snack_prune_regrow, which keep the copy current) until
+ * snack_values() is called again.  The paper has no counterpart to this
+ * call; it exists only for the column-ordered copy.
+ */
+snack_status snack_values_changed(snack_handle h, void *stream);
 
 /*
  * Copy the stored entries out in canonical order: row, col [nnz] int32 and

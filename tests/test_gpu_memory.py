@@ -21,13 +21,14 @@ def test_handle_bytes_follow_nnz(sparsity):
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     acct = m.snack_device_bytes(h)
-    # indices, values and both layouts: 20 B per stored entry, plus per line
-    # an offset, a segment record and a 256-float row of operand workspace
+    # indices, values in both orders and both layouts: 24 B per stored
+    # entry, plus per line an offset, a segment record and a 256-float row of
+    # operand workspace
     per_line = 4 + 16 + 256 * 4
-    assert 20 * nnz <= acct <= 21 * nnz + per_line * (out + inp) + (1 << 20)
+    assert 24 * nnz <= acct <= 25 * nnz + per_line * (out + inp) + (1 << 20)
     # what the device really gave up (allocation granularity included)
     assert free0 - free1 <= acct + (64 << 20)
-    # against the dense W alone (4 B per cell): ~0.5x at 90 %, ~0.09x at 99 %
+    # against the dense W alone (4 B per cell): ~0.6x at 90 %, ~0.1x at 99 %
     dense = 4 * out * inp
-    assert acct < {90: 0.6, 99: 0.1}[sparsity] * dense
+    assert acct < {90: 0.7, 99: 0.12}[sparsity] * dense
     del h

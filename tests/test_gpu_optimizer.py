@@ -61,8 +61,20 @@ class Case:
         return X, dY, g, S
 
     def values(self):
+        # read-only copy (a snack_values() view would hand out a writable
+        # pointer and stop the handle's column-ordered value copy)
         torch.cuda.synchronize()
-        return sn().snack_values(self.h).cpu().numpy().copy()
+        return sn().snack_export(self.h)[2]
+
+    def check_dx(self, B):
+        # dX reads the column-ordered copy the fused steps keep current
+        dY = self.g.standard_normal((B, self.out)).astype(np.float32)
+        dX = sn().snack_backward_input(self.h, to_dev(dY))
+        torch.cuda.synchronize()
+        r = self.ref
+        want, S = oracle.backward_input(self.out, self.inp, r["row"], r["col"], self.values(), dY)
+        got = dX.cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(got - want) <= TOL * S + 1e-30)
 
     def state(self, which):
         try:
@@ -118,6 +130,7 @@ def test_sgd_plain_and_momentum(B):
     c.sgd(B, 0.05, 0.0, 0.0)
     for _ in range(3):
         c.sgd(B, 0.05, 0.9, 1e-3)
+    c.check_dx(B)
     assert sn().snack_device_error(c.h) == 0
 
 
@@ -129,6 +142,7 @@ def test_adam_steps(shape, B):
     c = _uniform_case(*shape, 31)
     for t in (1, 2, 3):
         c.adam(B, t, wd=1e-4 if t == 3 else 0.0)
+    c.check_dx(min(B, 64))
     assert sn().snack_device_error(c.h) == 0
 
 
@@ -161,6 +175,7 @@ def test_state_follows_entries_through_prune_regrow():
     # and the next step runs on the new layout
     c.ref = canonical(c.out, c.inp, r1, c1, c.values())
     c.adam(16, 3)
+    c.check_dx(16)
 
 
 def test_invalid_optimizer_arguments():

@@ -256,6 +256,32 @@ def test_device_pointer_input_and_side_stream():
     assert_close("Y", Y, Yo, Sy)
 
 
+def test_column_ordered_value_copy_follows_writes():
+    # dX streams a column-ordered copy of the values while the library owns
+    # every write; a writable view switches it to the permutation path until
+    # snack_values_changed() re-derives the copy.  Resident (batch 1) and
+    # segment (batch 16) kernels, standalone and fused backward.
+    m = sn()
+    L = workloads.workload("gpt2_mlp").layers[0]
+    row, col, val = L.coo()
+    ref = canonical(L.out, L.inp, row, col, val)
+    h = m.snack_create(L.out, L.inp, row, col, val)
+
+    def check(vals):
+        for B in (1, 16):
+            X, dY = L.activations(B)
+            check_products(h, L.out, L.inp, dict(ref, val=vals), X, dY)
+    check(ref["val"])                              # copy current since creation
+    v = m.snack_values(h)
+    v.mul_(-0.5)                                   # written through the view
+    check(ref["val"] * np.float32(-0.5))           # permutation path
+    m.snack_values_changed(h)
+    check(ref["val"] * np.float32(-0.5))           # copy re-derived
+    v.add_(1.0)                                    # a write the handle is not told of
+    m.snack_values(h)                              # ... until the view is taken again
+    check(ref["val"] * np.float32(-0.5) + np.float32(1.0))
+
+
 def test_values_view_updates_in_place():
     L = workloads.workload("toy256").layers[0]
     row, col, val = L.coo()
