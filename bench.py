@@ -328,6 +328,9 @@ def run_ours(args):
                         ts.append((e0, e1))
                     torch.cuda.synchronize()
                     del g_op
+                    if op == "adam_step":  # the steps changed the values: re-derive
+                        sn.snack_values_changed(c["h"])  # their column-ordered copy
+                        torch.cuda.synchronize()
                     us = statistics.mean(a.elapsed_time(b) for a, b in ts) * 1e3
                     nbytes = metric_bytes(op, L.nnz, L.out, L.inp, B)
                     plan_op = {"fwd": 0, "bwd_input": 1}.get(op, 2)  # dW and Adam: rows
@@ -503,6 +506,8 @@ def run_only_op(args):
     import coo_spmm_sparse_gb300 as sn
     wl, cases = make_cases(args.workload, args.batches, args.seed)
     c = cases[0]
+    if args.layer:
+        c = next(x for x in cases if x["layer"].name == args.layer)
     L = c["layer"]
     B = sorted(c["acts"])[0]
     X, dY = (torch.from_numpy(a).cuda() for a in c["acts"][B])
@@ -575,9 +580,11 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-op", choices=["fwd", "bwd_input", "bwd_weight", "bwd"], default=None,
-                    help="profiling mode: run one op --reps times on the first layer and "
-                         "batch of the workload (cold L2 before each), print no JSON")
+                    help="profiling mode: run one op --reps times on one layer (--layer) and "
+                         "the first batch of the workload (cold L2 before each), print no JSON")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--layer", default=None,
+                    help="profiling mode: the workload's layer to run (default: its first)")
     ap.add_argument("--memory-sweep", action="store_true",
                     help="print the layer's device bytes against dense W at hidden 10000, "
                          "input 5000-25000, sparsity 90/95/99 %% (one JSON object)")

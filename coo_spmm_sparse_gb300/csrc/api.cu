@@ -74,8 +74,8 @@ void account(snack::Layer &L) {
   b += (size_t)std::max(L.csr.nslots, L.csc.nslots) * snack::kMaxSlice * 4;
   b += (size_t)std::max(L.csr.nsplit, L.csc.nsplit) * 4;
   b += (size_t)(L.pan_csr.ncta + 1 + L.pan_csc.ncta + 1) * 4 + 4;  // panels, error flag
-  // column-ordered values; optimizer state, gradient buffer, copy positions
-  const void *extra[] = {L.d_val_csc, L.d_opt[0], L.d_opt[1], L.d_gacc, L.d_csc_pos};
+  // column-ordered values; optimizer state, gradient buffer
+  const void *extra[] = {L.d_val_csc, L.d_opt[0], L.d_opt[1], L.d_gacc};
   for (const void *p : extra)
     if (p) b += (size_t)L.nnz_pad * 4;
   L.device_bytes = b;
@@ -277,16 +277,6 @@ snack_status run_opt_step(snack_handle h, const float *X, const float *dY, int64
   o.s0 = L.d_opt[0];
   o.s1 = o.kind == snack::kOptAdam ? L.d_opt[1] : nullptr;
   if (o.kind == snack::kOptSgd && o.mom == 0.f) o.s0 = nullptr;
-  if (L.csc_vals) {  // keep the column-ordered copy of the values current
-    if (!L.d_csc_pos) {
-      std::string err;
-      snack_status st = snack::build_csc_pos(L, s, err);
-      if (st != SNACK_OK) return fail(h, st, err);
-      account(L);
-    }
-    o.val_csc = L.d_val_csc;
-    o.csc_pos = L.d_csc_pos;
-  }
   snack_status st;
   for (int64_t b0 = 0; b0 < batch; b0 += kStepSlice) {
     const int nb = (int)std::min<int64_t>(kStepSlice, batch - b0);
@@ -299,6 +289,11 @@ snack_status run_opt_step(snack_handle h, const float *X, const float *dY, int64
     }
     if (st != SNACK_OK) return st;
   }
+  // The values changed: the column-ordered copy is stale (dX reads through
+  // the permutation) until snack_values_changed() re-derives it.  Keeping it
+  // current inside the step (a scattered 4-byte store per entry) measured
+  // slower than the permutation path it saves.
+  L.csc_vals = false;
   return SNACK_OK;
 }
 

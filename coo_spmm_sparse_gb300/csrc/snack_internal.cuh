@@ -8,8 +8,8 @@
 //   csc_row  [nnz_pad] int32   row of the s-th entry in (col, row) order
 //   csc_perm [nnz_pad] int32   canonical k of the s-th entry in (col, row) order
 //   val_csc  [nnz_pad] fp32    val[csc_perm[s]]: the values in (col, row) order,
-//                              kept equal to val while the library owns every
-//                              write to the values (see Layer::csc_vals)
+//                              trusted while the values have not changed since
+//                              it was derived (see Layer::csc_vals)
 //   col_ptr  [in+1]    int32   CSC index pointer
 //   seg_csr / seg_csc  int4    work decomposition of rows / columns into
 //                              segments {line, begin, end, split_id}
@@ -69,7 +69,6 @@ struct Layer {
   float *d_val_csc = nullptr;      // [nnz_pad] values in (col, row) order
   bool csc_vals = false;           // d_val_csc equals val through csc_perm
   bool values_shared = false;      // a writable values pointer is out (snack_values)
-  int32_t *d_csc_pos = nullptr;    // [nnz_pad] csc slot of canonical entry k (fused steps)
   int32_t *d_col_ptr = nullptr;
   SegTable csr, csc;
   // workspace
@@ -115,8 +114,6 @@ struct OptArgs {
   float *s0 = nullptr;                            // momentum buffer / first moment (or null)
   float *s1 = nullptr;                            // second moment (Adam)
   const float *gacc = nullptr;                    // gradient of earlier batch slices (or null)
-  float *val_csc = nullptr;                       // column-ordered copy to keep current (or null)
-  const int32_t *csc_pos = nullptr;               // [nnz] its slot of each canonical entry
 };
 
 struct SddmmArgs {
@@ -179,8 +176,6 @@ void free_layer(Layer &L);
 // val_csc[s] = val[csc_perm[s]]; the copy is current unless a writable
 // values pointer is out.
 snack_status refresh_csc_values(Layer &L, cudaStream_t s, std::string &err);
-// csc_pos[csc_perm[s]] = s (allocated on first use).
-snack_status build_csc_pos(Layer &L, cudaStream_t s, std::string &err);
 
 // Device memory helper: cudaMalloc with byte accounting.
 template <typename T>

@@ -502,11 +502,6 @@ __device__ __forceinline__ void opt_store(const OptArgs &o, int kq, OptQuad &q,
     store4(o.s1 + kq, q.mask, q.s1);
   }
   store4(o.val + kq, q.mask, q.w);
-  if (o.val_csc) {  // the column-ordered copy: scattered, fire-and-forget stores
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if ((q.mask >> e) & 1u) o.val_csc[o.csc_pos[kq + e]] = q.w[e];
-  }
 }
 
 // Column quads at kb (and kb + 4 * npt when QPS = 2), each only if it

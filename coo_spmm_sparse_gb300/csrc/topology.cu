@@ -296,11 +296,6 @@ __global__ void gather_by_perm(const int32_t *perm, const float *val, int64_t n,
   if (s < n) out[s] = val[perm[s]];
 }
 
-__global__ void invert_perm(const int32_t *perm, int64_t n, int32_t *pos) {
-  const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (s < n) pos[perm[s]] = (int32_t)s;
-}
-
 __global__ void finish_csc(const uint64_t *key, const uint32_t *src, int64_t n, int64_t out,
                            int32_t *csc_row, int32_t *csc_perm) {
   const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -424,7 +419,6 @@ snack_status finish_layout(Layer &L, const uint64_t *d_cell_key, cudaStream_t s,
   {
     snack_status st = refresh_csc_values(L, s, err);
     if (st != SNACK_OK) return st;
-    if (L.d_csc_pos && (st = build_csc_pos(L, s, err)) != SNACK_OK) return st;
   }
   std::vector<int32_t> rp(L.out + 1), cp(L.in + 1);
   TRY_CUDA(cudaMemcpyAsync(rp.data(), L.d_row_ptr, rp.size() * 4, cudaMemcpyDeviceToHost, s));
@@ -827,24 +821,12 @@ snack_status refresh_csc_values(Layer &L, cudaStream_t s, std::string &err) {
   return SNACK_OK;
 }
 
-snack_status build_csc_pos(Layer &L, cudaStream_t s, std::string &err) {
-  if (!L.d_csc_pos) {
-    TRY_CUDA(dev_alloc(&L.d_csc_pos, L.nnz_pad, (size_t *)nullptr));
-    TRY_CUDA(cudaMemsetAsync(L.d_csc_pos, 0, L.nnz_pad * 4, s));
-  }
-  if (L.nnz > 0) {
-    invert_perm<<<grid_for(L.nnz, 256), 256, 0, s>>>(L.d_csc_perm, L.nnz, L.d_csc_pos);
-    TRY_CUDA(cudaGetLastError());
-  }
-  return SNACK_OK;
-}
-
 void free_layer(Layer &L) {
   void *ptrs[] = {L.d_col,     L.d_row,     L.d_val,         L.d_row_ptr,     L.d_csc_row,
                   L.d_csc_perm, L.d_col_ptr, L.csr.d_seg,     L.csr.d_split,   L.csc.d_seg,
                   L.csc.d_split, L.d_xt,     L.d_dyt,         L.d_partial,     L.d_counter,
                   L.pan_csr.d_ptr, L.pan_csc.d_ptr, L.d_err,   L.d_opt[0],      L.d_opt[1],
-                  L.d_gacc,    L.d_val_csc, L.d_csc_pos};
+                  L.d_gacc,    L.d_val_csc};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   L = Layer();

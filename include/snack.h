@@ -146,7 +146,8 @@ snack_status snack_backward(snack_handle h, const float *X, const float *dY, flo
  *                             / (sqrt(v_k) / sqrt(1 - beta2^t) + eps)
  * (the conventions of torch.optim.SGD without dampening and torch.optim.Adam).
  * Values change in place: compute dX (snack_backward_input, which reads
- * them) before the step.
+ * them) before the step.  The column-ordered value copy becomes stale (see
+ * snack_values).
  *
  * State: nnz-long fp32 arrays owned by the handle, in canonical order
  * (snack_optimizer_state).  The first step that needs them allocates and
@@ -199,21 +200,25 @@ snack_status snack_prune_regrow(snack_handle h, float prune_frac, uint64_t seed,
  * valid until snack_destroy().
  *
  * The handle also keeps the values in column order, so that dX streams them
- * instead of reading each through the column permutation.  Handing out this
- * writable pointer makes that copy untrusted: from this call on, dX reads
- * the values through the permutation (same results, slower) until
- * snack_values_changed() is called.
+ * instead of reading each through the column permutation (creation and
+ * snack_prune_regrow derive it).  It is trusted only while the values stay
+ * as they were when it was derived: handing out this writable pointer, or a
+ * fused optimizer step, makes it stale, and dX then reads the values through
+ * the permutation (same results, slower) until snack_values_changed().
+ * Layers whose values stay fixed across many backward calls (a frozen layer,
+ * repeated evaluation) gain from calling it once.
  */
 snack_status snack_values(snack_handle h, float **dev_val);
 
 /*
- * Tell the handle that the caller has finished writing the values through
- * the snack_values() pointer: re-derives the column-ordered copy
- * (asynchronous on `stream`) and lets dX use it again.  The library then
- * assumes the values change only through its own calls (snack_sgd_step,
- * snack_adam_step, snack_prune_regrow, which keep the copy current) until
- * snack_values() is called again.  The paper has no counterpart to this
- * call; it exists only for the column-ordered copy.
+ * Tell the handle that the values will not change for a while (the caller
+ * has finished writing them through the snack_values() pointer, or a run of
+ * fused optimizer steps is over): re-derives the column-ordered copy
+ * (asynchronous on `stream`, one gather of the values) and lets dX stream
+ * it.  The library then assumes the values change only through its own
+ * calls until snack_values() is called again; a fused optimizer step makes
+ * the copy stale again.  The paper has no counterpart to this call; it
+ * exists only for the column-ordered copy.
  */
 snack_status snack_values_changed(snack_handle h, void *stream);
 

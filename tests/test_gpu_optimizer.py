@@ -67,14 +67,19 @@ class Case:
         return sn().snack_export(self.h)[2]
 
     def check_dx(self, B):
-        # dX reads the column-ordered copy the fused steps keep current
+        # after fused steps dX reads the values through the column permutation
+        # (their column-ordered copy is stale); after snack_values_changed()
+        # it streams the re-derived copy
         dY = self.g.standard_normal((B, self.out)).astype(np.float32)
-        dX = sn().snack_backward_input(self.h, to_dev(dY))
-        torch.cuda.synchronize()
         r = self.ref
         want, S = oracle.backward_input(self.out, self.inp, r["row"], r["col"], self.values(), dY)
-        got = dX.cpu().numpy().astype(np.float64)
-        assert np.all(np.abs(got - want) <= TOL * S + 1e-30)
+        for refresh in (False, True):
+            if refresh:
+                sn().snack_values_changed(self.h)
+            dX = sn().snack_backward_input(self.h, to_dev(dY))
+            torch.cuda.synchronize()
+            got = dX.cpu().numpy().astype(np.float64)
+            assert np.all(np.abs(got - want) <= TOL * S + 1e-30), refresh
 
     def state(self, which):
         try:
