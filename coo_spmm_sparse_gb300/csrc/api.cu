@@ -73,7 +73,7 @@ void account(snack::Layer &L) {
   b += (size_t)(L.in + L.out) * snack::kMaxSlice * 4;
   b += (size_t)std::max(L.csr.nslots, L.csc.nslots) * snack::kMaxSlice * 4;
   b += (size_t)std::max(L.csr.nsplit, L.csc.nsplit) * 4;
-  b += (size_t)(L.pan_csr.ncta + 1 + L.pan_csc.ncta + 1) * 4 + 4;  // panels, error flag
+  b += 4;  // error flag
   // column-ordered values; optimizer state, gradient buffer
   const void *extra[] = {L.d_val_csc, L.d_opt[0], L.d_opt[1], L.d_gacc};
   for (const void *p : extra)

@@ -46,19 +46,9 @@ struct SegTable {
   int4 *d_split = nullptr; // [nsplit]
 };
 
-// Lines of a segmentation grouped into one panel per SM (about nnz / #SMs
-// entries each) for the panel x tile kernels.
-struct Panels {
-  int32_t *d_ptr = nullptr;  // [ncta + 1] first line of each panel
-  int ncta = 0;
-  int max_lines = 0;
-};
-
 struct Layer {
   int64_t out = 0, in = 0, nnz = 0, nnz_pad = 0;
   int device = 0;
-  int sms = 0;                 // SM count of the device
-  Panels pan_csr, pan_csc;
   int *d_err = nullptr;        // device error flag (a bounded wait gave up)
   int32_t *d_col = nullptr;
   int32_t *d_row = nullptr;

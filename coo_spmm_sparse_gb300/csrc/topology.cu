@@ -333,39 +333,6 @@ void build_segments(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz
   t.nslots = slots;
 }
 
-// Host: group lines into `ncta` panels of about equal cost (entries plus a
-// small per-line charge), for the panel x tile kernels.
-snack_status build_panels(const std::vector<int32_t> &ptr, int64_t nlines, int ncta, Panels &pan,
-                          cudaStream_t s, std::string &err) {
-  if (pan.d_ptr) cudaFree(pan.d_ptr);
-  pan.d_ptr = nullptr;
-  pan.ncta = 0;
-  pan.max_lines = 0;
-  if (ncta < 1) return SNACK_OK;
-  std::vector<int32_t> p(ncta + 1, 0);
-  const double total = (double)ptr[nlines] + 4.0 * (double)nlines;
-  int64_t l = 0;
-  double cum = 0.0;
-  for (int i = 1; i < ncta; ++i) {
-    const double target = total * i / ncta;
-    while (l < nlines && cum + (ptr[l + 1] - ptr[l]) + 4.0 <= target) {
-      cum += (ptr[l + 1] - ptr[l]) + 4.0;
-      ++l;
-    }
-    p[i] = (int32_t)l;
-  }
-  p[ncta] = (int32_t)nlines;
-  int mx = 0;
-  for (int i = 0; i < ncta; ++i) mx = std::max(mx, p[i + 1] - p[i]);
-  TRY_CUDA(cudaMalloc(&pan.d_ptr, (ncta + 1) * sizeof(int32_t)));
-  TRY_CUDA(cudaMemcpyAsync(pan.d_ptr, p.data(), (ncta + 1) * sizeof(int32_t),
-                           cudaMemcpyHostToDevice, s));
-  TRY_CUDA(cudaStreamSynchronize(s));
-  pan.ncta = ncta;
-  pan.max_lines = mx;
-  return SNACK_OK;
-}
-
 snack_status upload_segments(const std::vector<int4> &seg, const std::vector<int4> &split,
                              SegTable &t, size_t *acct, cudaStream_t s, std::string &err) {
   if (t.d_seg) cudaFree(t.d_seg);
@@ -431,8 +398,6 @@ snack_status finish_layout(Layer &L, const uint64_t *d_cell_key, cudaStream_t s,
   build_segments(cp, L.in, n, seg, split, L.csc);
   st = upload_segments(seg, split, L.csc, &L.device_bytes, s, err);
   if (st != SNACK_OK) return st;
-  if ((st = build_panels(rp, L.out, L.sms, L.pan_csr, s, err)) != SNACK_OK) return st;
-  if ((st = build_panels(cp, L.in, L.sms, L.pan_csc, s, err)) != SNACK_OK) return st;
   // Split workspace: partial slots and re-armed tickets (zero between calls).
   if (L.d_partial) cudaFree(L.d_partial);
   if (L.d_counter) cudaFree(L.d_counter);
@@ -690,11 +655,6 @@ snack_status build_topology(Layer &L, int64_t nnz, const int32_t *d_row_user,
   TRY_CUDA(dev_alloc(&L.d_dyt, (size_t)L.out * kMaxSlice, acct));
   TRY_CUDA(dev_alloc(&L.d_err, 1, acct));
   TRY_CUDA(cudaMemsetAsync(L.d_err, 0, sizeof(int), s));
-  {
-    int dev = 0;
-    TRY_CUDA(cudaGetDevice(&dev));
-    TRY_CUDA(cudaDeviceGetAttribute(&L.sms, cudaDevAttrMultiProcessorCount, dev));
-  }
   TRY_CUDA(cudaMemsetAsync(L.d_col, 0, L.nnz_pad * 4, s));
   TRY_CUDA(cudaMemsetAsync(L.d_row, 0, L.nnz_pad * 4, s));
   TRY_CUDA(cudaMemsetAsync(L.d_val, 0, L.nnz_pad * 4, s));
@@ -825,7 +785,7 @@ void free_layer(Layer &L) {
   void *ptrs[] = {L.d_col,     L.d_row,     L.d_val,         L.d_row_ptr,     L.d_csc_row,
                   L.d_csc_perm, L.d_col_ptr, L.csr.d_seg,     L.csr.d_split,   L.csc.d_seg,
                   L.csc.d_split, L.d_xt,     L.d_dyt,         L.d_partial,     L.d_counter,
-                  L.pan_csr.d_ptr, L.pan_csc.d_ptr, L.d_err,   L.d_opt[0],      L.d_opt[1],
+                  L.d_err,     L.d_opt[0],  L.d_opt[1],
                   L.d_gacc,    L.d_val_csc};
   for (void *p : ptrs)
     if (p) cudaFree(p);
