@@ -137,7 +137,7 @@ snack_status run_forward(snack_handle h, const float *X, float *Y, int64_t batch
       op = L.d_xt;
     }
     const snack::SpmmArgs a = spmm_args(L, true, op, Y + b0 * L.out, nb);
-    cudaError_t e = snack::resident_fits(p.bw, L.in, L.csr.nseg)
+    cudaError_t e = snack::resident_fits(p.bw, L.in, L.csr.nseg, L.nnz)
                         ? snack::launch_resident_spmm(false, p, a, L.in, L.d_err, true, s)
                         : snack::launch_spmm_rows(p, a, true, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "forward launch");
@@ -194,8 +194,8 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     if (opt) rows.opt = *opt;
   }
   cudaError_t e;
-  const bool res_c = dX && snack::resident_fits(pc.bw, L.out, L.csc.nseg);
-  const bool res_r = want_w && !fused_opt && snack::resident_fits(pr.bw, L.in, L.csr.nseg);
+  const bool res_c = dX && snack::resident_fits(pc.bw, L.out, L.csc.nseg, L.nnz);
+  const bool res_r = want_w && !fused_opt && snack::resident_fits(pr.bw, L.in, L.csr.nseg, L.nnz);
   if (fused_opt) {  // the optimizer step has its own kernel
     e = snack::launch_sddmm_step(pr, rows, true, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "optimizer step launch");
@@ -596,7 +596,7 @@ snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_wi
   if (lanes_per_segment) *lanes_per_segment = p.lanes;
   if (segments) *segments = t.nseg;
   if (resident)
-    *resident = snack::resident_fits(p.bw, op == 1 ? h->L.out : h->L.in, t.nseg) ? 1 : 0;
+    *resident = snack::resident_fits(p.bw, op == 1 ? h->L.out : h->L.in, t.nseg, h->L.nnz) ? 1 : 0;
   return SNACK_OK;
 }
 

@@ -128,10 +128,14 @@ cudaError_t launch_resident(K kern, const A &a, int64_t n_op, int *err, size_t s
 
 }  // namespace
 
-// Slices of 1-4 floats whose whole operand fits in 192 KB, with at least two
-// segments per SM to spread.
-bool resident_fits(int bw, int64_t n_op, int64_t nseg) {
-  return bw <= 4 && n_op * bw * 4 <= kResidentMaxBytes && nseg >= 2 * (int64_t)sm_count();
+// Slices of 1-4 floats whose whole operand fits in 192 KB, on layers of at
+// least 2^22 entries whose value bytes cover the staging copies (one operand
+// per SM).  Measured on GB300: on smaller layers (e.g. 1 M entries at 10000
+// lines, or the 118 k-entry GPT-2 MLP layers) the segment kernels with the
+// stream look-ahead are faster, the copies being a large part of the traffic.
+bool resident_fits(int bw, int64_t n_op, int64_t nseg, int64_t nnz) {
+  return bw <= 4 && n_op * bw * 4 <= kResidentMaxBytes && nseg >= 2 * (int64_t)sm_count() &&
+         nnz >= (int64_t(1) << 22) && (int64_t)sm_count() * n_op * bw <= nnz;
 }
 
 cudaError_t launch_resident_spmm(bool perm, const Plan &p, const SpmmArgs &args, int64_t n_op,

@@ -140,7 +140,7 @@ cudaError_t launch_backward_fused(const Plan &pc, const SpmmArgs &cols, const Pl
 // Variants with the whole operand resident in shared memory (slices of 1-4
 // floats; resident_operand.cu).  n_op = operand lines (in for the forward
 // and dW, out for dX); err = the layer's device error flag.
-bool resident_fits(int bw, int64_t n_op, int64_t nseg);
+bool resident_fits(int bw, int64_t n_op, int64_t nseg, int64_t nnz);
 cudaError_t launch_resident_spmm(bool perm, const Plan &p, const SpmmArgs &a, int64_t n_op,
                                  int *err, bool pdl, cudaStream_t s);
 cudaError_t launch_resident_sddmm(const Plan &p, const SddmmArgs &a, int64_t n_op, int *err,

@@ -139,6 +139,28 @@ def test_large99_full_oracle_b16():
     check_products(h, L.out, L.inp, ref, X, dY, fused=False)
 
 
+# ------------------------------------------------------------ resident operand
+
+def test_resident_operand_full_oracle():
+    # 3000 x 3000 at 47 %: 4.23 M entries, enough for the kernels that stage
+    # the whole transposed operand in shared memory (slices of 1-4); full
+    # oracle for every product, fused backward included.
+    out = inp = 3000
+    nnz = workloads.nnz_for(out, inp, 53)
+    row, col = workloads.uniform_pattern(out, inp, nnz, 13)
+    val = workloads.normal(nnz, 0.05, 13, 0)
+    ref = canonical(out, inp, row, col, val)
+    h = sn().snack_create(out, inp, row, col, val)
+    for op in (0, 1, 2):
+        assert sn().snack_plan(h, op, 4, with_resident=True)[3] == 1
+    g = np.random.default_rng(14)
+    for B in (1, 2, 3, 4):
+        X = g.standard_normal((B, inp)).astype(np.float32)
+        dY = g.standard_normal((B, out)).astype(np.float32)
+        check_products(h, out, inp, ref, X, dY)
+    assert sn().snack_device_error(h) == 0
+
+
 # ------------------------------------------------------------ dense-ish layer
 
 def test_dense_lines_full_oracle():
@@ -330,11 +352,15 @@ def test_plan_follows_batch_and_row_length():
                  (129, 256), (300, 256)):
         assert sn().snack_plan(h, 0, B)[0] == w
     assert sn().snack_plan(h, 0, 16)[1] == 32            # 100 entries per row
-    # the whole 10000-line operand (40-160 KB) is staged in shared memory up
-    # to 4-wide slices; wider slices gather from global memory
-    assert sn().snack_plan(h, 0, 1, with_resident=True)[3] == 1
-    assert sn().snack_plan(h, 1, 4, with_resident=True)[3] == 1
-    assert sn().snack_plan(h, 0, 16, with_resident=True)[3] == 0
+    # a 1 M-entry layer gathers its operand from global memory at every
+    # width; a 5 M-entry one stages the whole 10000-line operand in shared
+    # memory while its copies (one per SM) stay within the value bytes
+    assert sn().snack_plan(h, 0, 1, with_resident=True)[3] == 0
+    h5, _ = sn().snack_create_random(L.out, L.inp, 5 * L.nnz, 2)
+    assert sn().snack_plan(h5, 0, 1, with_resident=True)[3] == 1
+    assert sn().snack_plan(h5, 1, 2, with_resident=True)[3] == 1
+    assert sn().snack_plan(h5, 0, 4, with_resident=True)[3] == 0
+    assert sn().snack_plan(h5, 0, 16, with_resident=True)[3] == 0
     small = workloads.workload("toy256").layers[0]
     r, c, v = small.coo()
     h2 = sn().snack_create(small.out, small.inp, r, c, v)
