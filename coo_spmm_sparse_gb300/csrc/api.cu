@@ -114,6 +114,7 @@ snack::SpmmArgs spmm_args(snack::Layer &L, bool rows, const float *op, float *ds
   a.counter = L.d_counter;
   a.lps = 32;
   a.nval = L.nnz_pad;
+  a.prefetch = 0;
   return a;
 }
 
@@ -136,7 +137,8 @@ snack_status run_forward(snack_handle h, const float *X, float *Y, int64_t batch
       g_launches.fetch_add(1, std::memory_order_relaxed);
       op = L.d_xt;
     }
-    const snack::SpmmArgs a = spmm_args(L, true, op, Y + b0 * L.out, nb);
+    snack::SpmmArgs a = spmm_args(L, true, op, Y + b0 * L.out, nb);
+    a.prefetch = transposed;
     cudaError_t e = snack::resident_fits(p.bw, L.in, L.csr.nseg, L.nnz)
                         ? snack::launch_resident_spmm(false, p, a, L.in, L.d_err, true, s)
                         : snack::launch_spmm_rows(p, a, true, s);
@@ -180,7 +182,10 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     if (want_w) xt = L.d_xt;
   }
   snack::SpmmArgs cols;
-  if (dX) cols = spmm_args(L, false, dyt, dX + b0 * L.in, nb);
+  if (dX) {
+    cols = spmm_args(L, false, dyt, dX + b0 * L.in, nb);
+    cols.prefetch = transposed;
+  }
   snack::SddmmArgs rows;
   if (want_w) {
     rows.seg = L.csr.d_seg;
@@ -191,6 +196,7 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     rows.dw = dW;
     rows.accumulate = b0 > 0;
     rows.lps = 32;
+    rows.prefetch = transposed;
     if (opt) rows.opt = *opt;
   }
   cudaError_t e;

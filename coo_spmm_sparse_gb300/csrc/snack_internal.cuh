@@ -90,6 +90,7 @@ struct SpmmArgs {
   int *counter;
   int lps;              // lanes per segment team (set by the launcher)
   int64_t nval;         // floats in the padded value array (L2 prefetch bound)
+  int prefetch;         // pull the segments' streams into L2 while waiting on a transpose
 };
 
 // Optimizer step fused into the SDDMM epilogue (kind != kOptNone): the
@@ -115,6 +116,7 @@ struct SddmmArgs {
   float *dw;         // [nnz]
   int accumulate;    // add to dw instead of overwriting (batch slices > 0)
   int lps;           // lanes per segment team (set by the launcher)
+  int prefetch;      // pull the segments' column streams into L2 while waiting on a transpose
   OptArgs opt;       // fused optimizer step instead of writing dw
 };
 

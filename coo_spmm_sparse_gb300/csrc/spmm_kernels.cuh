@@ -657,18 +657,21 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, 
 
 template <int BW, int LPS, bool PERM>
 __global__ void __launch_bounds__(256) spmm_segments(const SpmmArgs a) {
-  // Index / value streams do not depend on the kernel this one may follow:
-  // start pulling them into L2 before waiting for it.
-  prefetch_segments(a.seg, a.nseg, a.idx, PERM ? (const void *)a.perm : (const void *)a.val, LPS,
-                    blockIdx.x, gridDim.x);
-  if (PERM) prefetch_share(a.val, a.nval, blockIdx.x, gridDim.x);
+  // Index / value streams do not depend on the transpose this kernel may
+  // follow: pull them into L2 while waiting for it (without one to wait
+  // for, the prefetch only delays the kernel's own loads).
+  if (a.prefetch) {
+    prefetch_segments(a.seg, a.nseg, a.idx, PERM ? (const void *)a.perm : (const void *)a.val,
+                      LPS, blockIdx.x, gridDim.x);
+    if (PERM) prefetch_share(a.val, a.nval, blockIdx.x, gridDim.x);
+  }
   griddep_wait();
   spmm_part<BW, LPS, PERM>(a, a.src, blockIdx.x, gridDim.x);
 }
 
 template <int BW, int LPS, bool OPT = false>
 __global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
-  prefetch_segments(a.seg, a.nseg, a.col, nullptr, LPS, blockIdx.x, gridDim.x);
+  if (a.prefetch) prefetch_segments(a.seg, a.nseg, a.col, nullptr, LPS, blockIdx.x, gridDim.x);
   griddep_wait();
   sddmm_part<BW, LPS, false, OPT>(a, a.xt, blockIdx.x, gridDim.x);
 }
@@ -682,14 +685,16 @@ __global__ void __launch_bounds__(256) sddmm_segments(const SddmmArgs a) {
 template <int BW, int LPS, bool PERM>
 __global__ void __launch_bounds__(256) backward_segments(const SpmmArgs cols, const SddmmArgs rows,
                                                          int cols_blocks) {
-  if ((int)blockIdx.x < cols_blocks) {
-    prefetch_segments(cols.seg, cols.nseg, cols.idx,
-                      PERM ? (const void *)cols.perm : (const void *)cols.val, LPS, blockIdx.x,
-                      cols_blocks);
-    if (PERM) prefetch_share(cols.val, cols.nval, blockIdx.x, cols_blocks);
-  } else {
-    prefetch_segments(rows.seg, rows.nseg, rows.col, nullptr, LPS, blockIdx.x - cols_blocks,
-                      gridDim.x - cols_blocks);
+  if (cols.prefetch) {  // waiting on the transpose: pull the streams into L2
+    if ((int)blockIdx.x < cols_blocks) {
+      prefetch_segments(cols.seg, cols.nseg, cols.idx,
+                        PERM ? (const void *)cols.perm : (const void *)cols.val, LPS, blockIdx.x,
+                        cols_blocks);
+      if (PERM) prefetch_share(cols.val, cols.nval, blockIdx.x, cols_blocks);
+    } else {
+      prefetch_segments(rows.seg, rows.nseg, rows.col, nullptr, LPS, blockIdx.x - cols_blocks,
+                        gridDim.x - cols_blocks);
+    }
   }
   griddep_wait();
   if ((int)blockIdx.x < cols_blocks)
