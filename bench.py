@@ -18,8 +18,8 @@ collective on the data path).
 
 Also reported: the roofline of the dominant op (metric bytes / measured
 duration against the measured HBM copy bandwidth), an end-to-end number
-through the same calls with host buffers (pinned H2D of X and dY, D2H of Y,
-dX and dW inside the timed region), the CPU oracle on the host cores on a
+through the same calls with host buffers (one pinned H2D copy of every X and
+dY, one D2H copy of every Y, dX and dW, inside the timed region), the CPU oracle on the host cores on a
 bounded sample, the SM clocks sampled during the timed region, and the
 kernel launches.  The per-op table also times the fused Adam step
 (snack_adam_step) of each layer and batch; it is not part of the metric.
@@ -350,28 +350,48 @@ def run_ours(args):
                 "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
                 "bytes": "metric bytes nnz*12 + dense operands, per launch"}
 
-    # End to end through the same calls with host buffers.
-    pinned = []
-    for c in cases:
-        for B, d in c["dev"].items():
-            pinned.append(dict(c=c, d=d, X=torch.from_numpy(c["acts"][B][0]).pin_memory(),
-                               dY=torch.from_numpy(c["acts"][B][1]).pin_memory(),
-                               Y=torch.empty(d["Y"].shape).pin_memory(),
-                               dX=torch.empty(d["dX"].shape).pin_memory(),
-                               dW=torch.empty(d["dW"].shape).pin_memory()))
-    h2d = sum(p["X"].numel() * 4 + p["dY"].numel() * 4 for p in pinned)
-    d2h = sum(p["Y"].numel() * 4 + p["dX"].numel() * 4 + p["dW"].numel() * 4 for p in pinned)
+    # End to end through the same calls with host buffers: each step's inputs
+    # (X, dY of every layer and batch) travel in one pinned buffer with one
+    # H2D copy, and its results (Y, dX, dW) come back in one D2H copy; every
+    # array sits at a 16-byte aligned offset of its buffer.
+    pairs = [(c, B, d) for c in cases for B, d in c["dev"].items()]
+
+    def layout(sizes):
+        offs, n = [], 0
+        for sz in sizes:
+            offs.append(n)
+            n += (sz + 3) & ~3
+        return offs, n
+
+    in_arrays = [(c["acts"][B][0], c["acts"][B][1]) for c, B, _ in pairs]
+    out_shapes = [(d["Y"].shape, d["dX"].shape, d["dW"].shape) for _, _, d in pairs]
+    in_off, n_in = layout([a.size for xs in in_arrays for a in xs])
+    out_off, n_out = layout([int(np.prod(sh)) for shs in out_shapes for sh in shs])
+    h_in = torch.empty(n_in, dtype=torch.float32).pin_memory()
+    h_out = torch.empty(n_out, dtype=torch.float32).pin_memory()
+    d_in = torch.empty(n_in, dtype=torch.float32, device=dev)
+    d_out = torch.empty(n_out, dtype=torch.float32, device=dev)
+    views = []
+    for i, ((c, B, d), (X, dY), shs) in enumerate(zip(pairs, in_arrays, out_shapes)):
+        h_in[in_off[2 * i]:in_off[2 * i] + X.size] = torch.from_numpy(X).reshape(-1)
+        h_in[in_off[2 * i + 1]:in_off[2 * i + 1] + dY.size] = torch.from_numpy(dY).reshape(-1)
+
+        def dview(buf, off, shape):
+            n = int(np.prod(shape))
+            return buf[off:off + n].view(*shape)
+        views.append(dict(h=c["h"], X=dview(d_in, in_off[2 * i], X.shape),
+                          dY=dview(d_in, in_off[2 * i + 1], dY.shape),
+                          Y=dview(d_out, out_off[3 * i], shs[0]),
+                          dX=dview(d_out, out_off[3 * i + 1], shs[1]),
+                          dW=dview(d_out, out_off[3 * i + 2], shs[2])))
+    h2d, d2h = n_in * 4, n_out * 4
 
     def e2e_step():
-        for p in pinned:
-            d = p["d"]
-            d["X"].copy_(p["X"], non_blocking=True)
-            d["dY"].copy_(p["dY"], non_blocking=True)
-            sn.snack_forward(p["c"]["h"], d["X"], d["Y"], stream=stream)
-            sn.snack_backward(p["c"]["h"], d["X"], d["dY"], d["dX"], d["dW"], stream=stream)
-            p["Y"].copy_(d["Y"], non_blocking=True)
-            p["dX"].copy_(d["dX"], non_blocking=True)
-            p["dW"].copy_(d["dW"], non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
+        for v in views:
+            sn.snack_forward(v["h"], v["X"], v["Y"], stream=stream)
+            sn.snack_backward(v["h"], v["X"], v["dY"], v["dX"], v["dW"], stream=stream)
+        h_out.copy_(d_out, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -416,8 +436,9 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
-                    "how": "per step: pinned H2D of X, dY; snack_forward + snack_backward "
-                           "via the C ABI (no graph); D2H of Y, dX, dW"},
+                    "how": "per step: one pinned H2D copy of every X and dY; snack_forward + "
+                           "snack_backward per layer and batch via the C ABI (no graph); one "
+                           "D2H copy of every Y, dX, dW"},
             "gpu_launches": int(launches_per_step * args.steps),
             "launches_per_step": int(launches_per_step),
             "clocks": clk,
