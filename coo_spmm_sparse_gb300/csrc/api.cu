@@ -115,7 +115,38 @@ snack::SpmmArgs spmm_args(snack::Layer &L, bool rows, const float *op, float *ds
   a.lps = 32;
   a.nval = L.nnz_pad;
   a.prefetch = 0;
+  a.stride = 0;  // set with the plan
+  a.nsub = 1;
   return a;
+}
+
+// Batch sub-slices for a table too small to fill the GPU: while its teams
+// would fill fewer blocks than there are SMs, the slice (width p.bw, the
+// transposed operand's row stride) is cut into sub-slices of half the
+// width, each covered by its own teams in the same launch (no combining:
+// they write different rows of the output).  Tables with split lines keep
+// whole slices, their partial sums being per slice.
+snack::Plan sub_slices(const snack::SegTable &t, const snack::Plan &p, int nb, int *nsub) {
+  *nsub = 1;
+  snack::Plan q = p;
+  if (t.nsplit != 0 || t.nseg == 0) return q;
+  const int64_t sms = snack::device_sms();
+  while (q.bw >= 16) {
+    const int64_t blocks = (t.nseg * *nsub * snack::plan_team_lanes(q) + 255) / 256;
+    if (blocks >= sms) break;
+    const snack::Plan h = snack::plan_for_width(t, q.bw / 2);
+    *nsub = (nb + h.bw - 1) / h.bw;
+    q = h;
+  }
+  return q;
+}
+
+// dX over the column segments: through the permutation, or (values in
+// column order) with the canonical-order kernels.
+cudaError_t launch_cols(const snack::Layer &L, const snack::Plan &p, snack::SpmmArgs a, int nb,
+                        cudaStream_t s) {
+  const snack::Plan q = sub_slices(L.csc, p, nb, &a.nsub);
+  return a.perm ? snack::launch_spmm_cols(q, a, true, s) : snack::launch_spmm_rows(q, a, true, s);
 }
 
 // Forward Y = X W^T over batch slices of at most 64: the slice of X is
@@ -139,19 +170,18 @@ snack_status run_forward(snack_handle h, const float *X, float *Y, int64_t batch
     }
     snack::SpmmArgs a = spmm_args(L, true, op, Y + b0 * L.out, nb);
     a.prefetch = transposed;
-    cudaError_t e = snack::resident_fits(p.bw, L.in, L.csr.nseg, L.nnz)
-                        ? snack::launch_resident_spmm(false, p, a, L.in, L.d_err, true, s)
-                        : snack::launch_spmm_rows(p, a, true, s);
+    a.stride = p.bw;
+    cudaError_t e;
+    if (snack::resident_fits(p.bw, L.in, L.csr.nseg, L.nnz)) {
+      e = snack::launch_resident_spmm(false, p, a, L.in, L.d_err, true, s);
+    } else {
+      const snack::Plan q = sub_slices(L.csr, p, nb, &a.nsub);
+      e = snack::launch_spmm_rows(q, a, true, s);
+    }
     if (e != cudaSuccess) return cuda_fail(h, e, "forward launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }
   return SNACK_OK;
-}
-
-// dX over the column segments: through the permutation, or (values in
-// column order) with the canonical-order kernels.
-cudaError_t launch_cols(const snack::Plan &p, const snack::SpmmArgs &a, cudaStream_t s) {
-  return a.perm ? snack::launch_spmm_cols(p, a, true, s) : snack::launch_spmm_rows(p, a, true, s);
 }
 
 // One batch slice of the backward: dX (if dX) and / or the weight product
@@ -185,6 +215,7 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
   if (dX) {
     cols = spmm_args(L, false, dyt, dX + b0 * L.in, nb);
     cols.prefetch = transposed;
+    cols.stride = pc.bw;
   }
   snack::SddmmArgs rows;
   if (want_w) {
@@ -215,7 +246,7 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     if (dX) {
       e = res_c ? snack::launch_resident_spmm(cols.perm != nullptr, pc, cols, L.out, L.d_err,
                                               true, s)
-                : launch_cols(pc, cols, s);
+                : launch_cols(L, pc, cols, nb, s);
       if (e != cudaSuccess) return cuda_fail(h, e, "backward-input launch");
       g_launches.fetch_add(1, std::memory_order_relaxed);
     }
@@ -230,7 +261,7 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
   if (dX && want_w)
     e = snack::launch_backward_fused(pc, cols, pr, rows, true, s);
   else if (dX)
-    e = launch_cols(pc, cols, s);
+    e = launch_cols(L, pc, cols, nb, s);
   else
     e = snack::launch_sddmm(pr, rows, true, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "backward launch");

@@ -44,8 +44,16 @@ int entry_lanes(int bw) { return lanes_for(bw); }
 // Team size: a group takes 4 entries per step; aim for about two steps per
 // group on an average segment, between 8 and 32 lanes.
 Plan choose_plan(const SegTable &t, int64_t nb) {
+  return plan_for_width(t, slice_width(nb < kMaxSlice ? nb : kMaxSlice));
+}
+
+int plan_team_lanes(const Plan &p) { return team_lanes(p); }
+
+int device_sms() { return sm_count(); }
+
+Plan plan_for_width(const SegTable &t, int bw) {
   Plan p;
-  p.bw = slice_width(nb < kMaxSlice ? nb : kMaxSlice);
+  p.bw = bw;
   const int g = lanes_for(p.bw);
   const double want = t.mean_len / 8.0;
   int npt = 1;

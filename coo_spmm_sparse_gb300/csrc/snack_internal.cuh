@@ -91,6 +91,9 @@ struct SpmmArgs {
   int lps;              // lanes per segment team (set by the launcher)
   int64_t nval;         // floats in the padded value array (L2 prefetch bound)
   int prefetch;         // pull the segments' streams into L2 while waiting on a transpose
+  int stride;           // floats between operand rows (the transposed slice's width)
+  int nsub;             // batch sub-slices of BW columns, one team per (sub-slice, segment);
+                        // > 1 only for tables without split lines
 };
 
 // Optimizer step fused into the SDDMM epilogue (kind != kOptNone): the
@@ -127,6 +130,9 @@ struct Plan {
 };
 int slice_width(int64_t nb);
 Plan choose_plan(const SegTable &t, int64_t nb);
+Plan plan_for_width(const SegTable &t, int bw);
+int plan_team_lanes(const Plan &p);  // lanes per team the launchers use
+int device_sms();                    // SM count of the current device
 int entry_lanes(int bw);
 
 // Launchers (spmm_*.cu).  Return the launch's cudaError_t.

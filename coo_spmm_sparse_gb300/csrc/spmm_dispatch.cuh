@@ -104,19 +104,23 @@ constexpr int half_team(int W, int L) {
 // = half_team lanes) can hold at once: then the last segments would run as
 // a second wave behind their teams' first ones, so `kh` runs instead with
 // every segment resident from the start.
+inline int64_t teams_of(const SpmmArgs &a) { return a.nseg * a.nsub; }
+inline int64_t teams_of(const SddmmArgs &a) { return a.nseg; }
+
 template <typename K, typename KH, typename A>
 inline cudaError_t launch_one_wave(K k, int L, KH kh, int LH, A a, bool pdl, cudaStream_t s) {
   const int64_t cap = resident_capacity(k);
+  const int64_t teams = teams_of(a);
   if (LH < L) {
     const int64_t cap_h = resident_capacity(kh);
-    if (a.nseg > cap * (256 / L) && a.nseg <= cap_h * (256 / LH)) {
+    if (teams > cap * (256 / L) && teams <= cap_h * (256 / LH)) {
       a.lps = LH;
-      const int64_t need = (a.nseg * LH + 255) / 256;
+      const int64_t need = (teams * LH + 255) / 256;
       return launch_ex(kh, need < cap_h ? need : cap_h, pdl, s, a);
     }
   }
   a.lps = L;
-  const int64_t need = (a.nseg * L + 255) / 256;
+  const int64_t need = (teams * L + 255) / 256;
   return launch_ex(k, need < cap ? need : cap, pdl, s, a);
 }
 

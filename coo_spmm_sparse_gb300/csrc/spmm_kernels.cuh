@@ -208,9 +208,9 @@ __device__ __forceinline__ void load_quad(const SpmmArgs &a, int kb, int k0, int
 }
 
 // Gather the lane's slice of the dense rows of Q quads (all loads issued
-// before any use), then accumulate.
+// before any use), then accumulate.  Operand row c starts at src + c * ld.
 template <int BW, int Q, bool SM = false>
-__device__ __forceinline__ void gather_fma(const float *src, const int (&c)[Q][4],
+__device__ __forceinline__ void gather_fma(const float *src, int ld, const int (&c)[Q][4],
                                            const float (&w)[Q][4], const bool (&ok)[Q][4],
                                            float (&acc)[SliceShape<BW>::NV][SliceShape<BW>::VEC]) {
   using S = SliceShape<BW>;
@@ -223,7 +223,7 @@ __device__ __forceinline__ void gather_fma(const float *src, const int (&c)[Q][4
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         if (ok[q][e]) {
-          load_op<VEC, SM>(src + (int64_t)c[q][e] * BW + v * G * VEC, x[q][e][v]);
+          load_op<VEC, SM>(src + (int64_t)c[q][e] * ld + v * G * VEC, x[q][e][v]);
         } else {
 #pragma unroll
           for (int i = 0; i < VEC; ++i) x[q][e][v][i] = 0.f;
@@ -240,6 +240,14 @@ __device__ __forceinline__ void gather_fma(const float *src, const int (&c)[Q][4
           // masked entries (a neighbouring line's) add exactly nothing, even
           // when their value is infinite or NaN
           acc[v][i] = fmaf(ok[q][e] ? w[q][e] : 0.f, x[q][e][v][i], acc[v][i]);
+}
+
+// The same for an operand whose rows are BW floats apart.
+template <int BW, int Q, bool SM = false>
+__device__ __forceinline__ void gather_fma(const float *src, const int (&c)[Q][4],
+                                           const float (&w)[Q][4], const bool (&ok)[Q][4],
+                                           float (&acc)[SliceShape<BW>::NV][SliceShape<BW>::VEC]) {
+  gather_fma<BW, Q, SM>(src, BW, c, w, ok, acc);
 }
 
 // Index and value quads of one step (at kb and kb + 4 * npt, each only if
@@ -272,8 +280,8 @@ __device__ __forceinline__ void load_step(const SpmmArgs &a, int kb, int k1, int
 // ahead the same way it measured slower at 64-wide slices, so it keeps the
 // plain loop.)
 template <int BW>
-__device__ __forceinline__ void walk_pipelined(const SpmmArgs &a, const float *src, int kb, int k0,
-                                               int k1, int npt,
+__device__ __forceinline__ void walk_pipelined(const SpmmArgs &a, const float *src, int ld, int kb,
+                                               int k0, int k1, int npt,
                                                float (&acc)[SliceShape<BW>::NV]
                                                            [SliceShape<BW>::VEC]) {
   int c[2][4] = {};
@@ -291,7 +299,7 @@ __device__ __forceinline__ void walk_pipelined(const SpmmArgs &a, const float *s
     int cn[2][4] = {};
     float wn[2][4] = {};
     load_step(a, kb + 8 * npt, k1, npt, cn, wn);
-    gather_fma<BW, 2, false>(src, c, w, ok, acc);
+    gather_fma<BW, 2, false>(src, ld, c, w, ok, acc);
 #pragma unroll
     for (int q = 0; q < 2; ++q)
 #pragma unroll
@@ -323,13 +331,20 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
   const int64_t stride = nblocks * teams_per_block;
   const int64_t my_team = block * teams_per_block + threadIdx.x / lps;
   const int64_t warp_team = block * teams_per_block + (threadIdx.x & ~31) / lps;
-  const float *src = op + sub * VEC;
+  // Batch sub-slices (nsub > 1, lines never split): team t works on segment
+  // t % nseg for the BW-wide sub-slice t / nseg of an operand whose rows are
+  // a.stride floats apart.
+  const int ld = SM ? BW : a.stride;
+  const int64_t nteams = a.nseg * a.nsub;
 
-  for (int64_t t0 = 0; warp_team + t0 < a.nseg; t0 += stride) {
+  for (int64_t t0 = 0; warp_team + t0 < nteams; t0 += stride) {
     const int64_t team = my_team + t0;
-    const bool active = team < a.nseg;
+    const bool active = team < nteams;
+    const int part_b = a.nsub > 1 && active ? (int)(team / a.nseg) : 0;
+    const int64_t segi = team - (int64_t)part_b * a.nseg;
+    const float *src = op + part_b * BW + sub * VEC;
     int4 sg = make_int4(0, 0, 0, -1);
-    if (active) sg = a.seg[team];
+    if (active) sg = a.seg[segi];
     const int k0 = sg.y, k1 = sg.z;
 
     float acc[NV][VEC];
@@ -340,7 +355,7 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
 
     int kb = (k0 & ~3) + 4 * grp;
     if constexpr (!SM && !PERM && PIPE) {
-      walk_pipelined<BW>(a, src, kb, k0, k1, npt, acc);
+      walk_pipelined<BW>(a, src, ld, kb, k0, k1, npt, acc);
     } else {
       for (; kb + 4 * npt < k1; kb += 8 * npt) {  // two quads in flight
         int c[2][4];
@@ -355,7 +370,7 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
             const int k = kb + q * 4 * npt + e;
             ok[q][e] = k >= k0 && k < k1;
           }
-        gather_fma<BW, 2, SM>(src, c, w, ok, acc);
+        gather_fma<BW, 2, SM>(src, ld, c, w, ok, acc);
       }
       if (kb < k1) {
         int c[1][4];
@@ -364,7 +379,7 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
         load_quad<PERM>(a, kb, k0, k1, c[0], w[0]);
 #pragma unroll
         for (int e = 0; e < 4; ++e) ok[0][e] = kb + e >= k0 && kb + e < k1;
-        gather_fma<BW, 1, SM>(src, c, w, ok, acc);
+        gather_fma<BW, 1, SM>(src, ld, c, w, ok, acc);
       }
     }
 
@@ -379,13 +394,15 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
     if (!active) continue;
     const int line = sg.x;
     if (sg.w < 0) {
-      if (grp == 0) store_line<BW>(a.dst, a.ld, a.nb, line, sub, acc);
+      if (grp == 0)
+        store_line<BW>(a.dst + (int64_t)part_b * BW * a.ld, a.ld, a.nb - part_b * BW, line, sub,
+                       acc);
       continue;
     }
 
     // Line split over several segments: park the partial, last arrival sums.
     const int4 sp = a.split[sg.w];  // {first segment, parts, first slot, 0}
-    const int part = (int)(team - sp.x);
+    const int part = (int)(segi - sp.x);
     if (grp == 0) {
       float *mine = a.partial + (int64_t)(sp.z + part) * BW + sub * VEC;
 #pragma unroll
