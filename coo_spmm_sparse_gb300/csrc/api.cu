@@ -141,6 +141,19 @@ snack::Plan sub_slices(const snack::SegTable &t, const snack::Plan &p, int nb, i
   return q;
 }
 
+// Entry sub-ranges for the SDDMM of a table too small to fill the GPU:
+// while its teams would fill fewer blocks than there are SMs, each segment
+// is cut into twice as many parts (of 16 or more entries on average), each
+// taken by its own team; the entries are independent, nothing is combined.
+int sddmm_subranges(const snack::SegTable &t, const snack::Plan &p) {
+  const int64_t sms = snack::device_sms();
+  const int64_t lanes = snack::plan_team_lanes(p);
+  int nsub = 1;
+  while (nsub < 8 && (t.nseg * nsub * lanes + 255) / 256 < sms && t.mean_len >= 32.0 * nsub)
+    nsub *= 2;
+  return nsub;
+}
+
 // dX over the column segments: through the permutation, or (values in
 // column order) with the canonical-order kernels.
 cudaError_t launch_cols(const snack::Layer &L, const snack::Plan &p, snack::SpmmArgs a, int nb,
@@ -228,11 +241,13 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     rows.accumulate = b0 > 0;
     rows.lps = 32;
     rows.prefetch = transposed;
+    rows.nsub = 1;
     if (opt) rows.opt = *opt;
   }
   cudaError_t e;
   const bool res_c = dX && snack::resident_fits(pc.bw, L.out, L.csc.nseg, L.nnz);
   const bool res_r = want_w && !fused_opt && snack::resident_fits(pr.bw, L.in, L.csr.nseg, L.nnz);
+  if (want_w && !res_r) rows.nsub = sddmm_subranges(L.csr, pr);
   if (fused_opt) {  // the optimizer step has its own kernel
     e = snack::launch_sddmm_step(pr, rows, true, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "optimizer step launch");

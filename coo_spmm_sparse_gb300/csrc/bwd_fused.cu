@@ -14,7 +14,7 @@ cudaError_t launch_backward_fused(const Plan &pc, const SpmmArgs &cols_in, const
   cols.lps = lps;
   rows.lps = lps;
   const int64_t need_c = (cols.nseg * lps + 255) / 256;
-  const int64_t need_r = (rows.nseg * lps + 255) / 256;
+  const int64_t need_r = (teams_of(rows) * lps + 255) / 256;
   if (need_c + need_r == 0) return cudaSuccess;
 #define SNACK_CALL(W, L)                                                            \
   {                                                                                 \

@@ -120,6 +120,7 @@ struct SddmmArgs {
   int accumulate;    // add to dw instead of overwriting (batch slices > 0)
   int lps;           // lanes per segment team (set by the launcher)
   int prefetch;      // pull the segments' column streams into L2 while waiting on a transpose
+  int nsub;          // entry sub-ranges per segment, one team each
   OptArgs opt;       // fused optimizer step instead of writing dw
 };
 

@@ -105,7 +105,7 @@ constexpr int half_team(int W, int L) {
 // a second wave behind their teams' first ones, so `kh` runs instead with
 // every segment resident from the start.
 inline int64_t teams_of(const SpmmArgs &a) { return a.nseg * a.nsub; }
-inline int64_t teams_of(const SddmmArgs &a) { return a.nseg; }
+inline int64_t teams_of(const SddmmArgs &a) { return a.nseg * a.nsub; }
 
 template <typename K, typename KH, typename A>
 inline cudaError_t launch_one_wave(K k, int L, KH kh, int LH, A a, bool pdl, cudaStream_t s) {

@@ -637,9 +637,19 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, 
   const int64_t teams_per_block = blockDim.x / lps;
   const int64_t stride = nblocks * teams_per_block;
   const float *xt = op + sub * VEC;
-  for (int64_t team = block * teams_per_block + threadIdx.x / lps; team < a.nseg; team += stride) {
-    const int4 sg = a.seg[team];
-    const int r = sg.x, k0 = sg.y, k1 = sg.z;
+  // Entry sub-ranges (nsub > 1): team t takes part t / nseg of segment
+  // t % nseg (the entries are independent, nothing to combine).
+  const int64_t nteams = a.nseg * a.nsub;
+  for (int64_t team = block * teams_per_block + threadIdx.x / lps; team < nteams; team += stride) {
+    const int part = a.nsub > 1 ? (int)(team / a.nseg) : 0;
+    const int4 sg = a.seg[team - (int64_t)part * a.nseg];
+    const int r = sg.x;
+    int k0 = sg.y, k1 = sg.z;
+    if (a.nsub > 1) {
+      const int64_t len = k1 - k0;
+      k1 = sg.y + (int)((part + 1) * len / a.nsub);
+      k0 = sg.y + (int)(part * len / a.nsub);
+    }
     float dy[NV][VEC];
     {
       const float *p = a.dyt + (int64_t)r * BW + sub * VEC;
