@@ -162,7 +162,7 @@ cudaError_t launch_cols(const snack::Layer &L, const snack::Plan &p, snack::Spmm
   return a.perm ? snack::launch_spmm_cols(q, a, true, s) : snack::launch_spmm_rows(q, a, true, s);
 }
 
-// Forward Y = X W^T over batch slices of at most 64: the slice of X is
+// Forward Y = X W^T over batch slices of at most 256: the slice of X is
 // transposed into the workspace (not needed for a single row), then the
 // row-segment kernel runs.  Every launch is a programmatic dependent of the
 // kernel before it on the stream (the caller's or this call's own): its
