@@ -33,7 +33,7 @@ __all__ = [
     "SnackError", "SnackHandle", "snack_create", "snack_create_random", "snack_forward",
     "snack_backward_input", "snack_backward_weight", "snack_backward", "snack_prune_regrow",
     "snack_values", "snack_values_changed", "snack_sgd_step", "snack_adam_step", "snack_optimizer_state", "snack_export", "snack_export_segments", "snack_plan", "snack_nnz",
-    "snack_device_bytes", "snack_destroy", "snack_launch_count", "snack_forward_csr_static", "snack_device_error", "SnackLinear", "library_path",
+    "snack_device_bytes", "snack_destroy", "snack_launch_count", "snack_forward_csr_static", "snack_device_error", "snack_selftest_wait", "SnackLinear", "library_path",
 ]
 
 
@@ -322,6 +322,14 @@ def snack_forward_csr_static(out: int, inp: int, row_ptr: torch.Tensor, col: tor
                                          _ptr(val) if nnz else None, _ptr(X), _ptr(Y), B,
                                          _stream(stream, X.device)))
     return Y
+
+
+def snack_selftest_wait(stream=None) -> int:
+    """Run the bounded-wait self-test (a wait nothing completes); returns 1
+    when the wait gave up as designed."""
+    flag = ctypes.c_int(0)
+    _check(_lib.snack_selftest_wait(_stream(stream), ctypes.byref(flag)))
+    return int(flag.value)
 
 
 def snack_device_error(h: SnackHandle) -> int:

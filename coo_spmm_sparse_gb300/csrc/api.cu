@@ -654,6 +654,25 @@ snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_wi
 
 uint64_t snack_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+snack_status snack_selftest_wait(void *stream, int *timed_out) {
+  if (!timed_out) return fail(nullptr, SNACK_ERR_INVALID_ARG, "timed_out is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int *d = nullptr;
+  cudaError_t e = cudaMalloc(&d, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "self-test flag allocation");
+  int v = 0;
+  if ((e = cudaMemsetAsync(d, 0, sizeof(int), s)) != cudaSuccess ||
+      (e = snack::launch_wait_selftest(d, s)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(&v, d, sizeof(int), cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(s)) != cudaSuccess) {
+    cudaFree(d);
+    return cuda_fail(nullptr, e, "self-test");
+  }
+  cudaFree(d);
+  *timed_out = v;
+  return SNACK_OK;
+}
+
 snack_status snack_device_error(snack_handle h, int *flag, void *stream) {
   if (!h || !flag) return fail(h, SNACK_ERR_INVALID_ARG, "NULL argument");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -25,11 +25,30 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Bounded wait for phase `parity` of the mbarrier at bar: true once it has
+// completed, false after `limit` polls (each poll may block for a
+// hardware-bounded time).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t it = 0; it <= limit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
 // Copy nfl floats from src (global, 16-byte aligned) into dst (this CTA's
 // shared memory): bulk copies for the 16-byte multiple, plain loads for the
-// last 0-3 floats.  A wait that does not complete within ~2^22 polls sets
-// *err and gives up, so the kernel always terminates.
-__device__ __forceinline__ void stage_operand(const float *src, int64_t nfl, float *dst,
+// last 0-3 floats.  Returns true (for the whole block) when the copy has
+// landed.  A wait that does not complete within ~2^22 polls sets *err, waits
+// once more (bounded) for the copies still in flight, and returns false:
+// the block then skips its work and exits, so the kernel always terminates.
+__device__ __forceinline__ bool stage_operand(const float *src, int64_t nfl, float *dst,
                                               uint64_t *bar, int *err) {
   const int64_t bulk = nfl & ~int64_t(3);
   if (threadIdx.x == 0) {
@@ -51,23 +70,15 @@ __device__ __forceinline__ void stage_operand(const float *src, int64_t nfl, flo
     }
   }
   for (int64_t i = bulk + threadIdx.x; i < nfl; i += blockDim.x) dst[i] = src[i];
-  if (bulk > 0) {
-    for (uint32_t it = 0;; ++it) {
-      uint32_t done;
-      asm volatile(
-          "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n"
-          " selp.u32 %0, 1, 0, p;\n}\n"
-          : "=r"(done)
-          : "r"(smem_u32(bar))
-          : "memory");
-      if (done) break;
-      if (it > (1u << 22)) {
-        atomicOr(err, 1);
-        break;
-      }
-    }
+  bool ok = true;
+  if (bulk > 0) ok = mbar_wait(bar, 0, 1u << 22);
+  ok = __syncthreads_and(ok);
+  if (!ok) {
+    if (threadIdx.x == 0) atomicOr(err, 1);
+    mbar_wait(bar, 0, 1u << 22);  // let copies still in flight land before the block exits
   }
   __syncthreads();
+  return ok;
 }
 
 template <int BW, int LPS, bool PERM>
@@ -76,7 +87,7 @@ __global__ void __launch_bounds__(kResidentThreads) spmm_resident(const SpmmArgs
   extern __shared__ __align__(128) float op_s[];
   __shared__ uint64_t bar;
   griddep_wait();
-  stage_operand(a.src, n_op * BW, op_s, &bar, err);
+  if (!stage_operand(a.src, n_op * BW, op_s, &bar, err)) return;
   spmm_part<BW, LPS, PERM, true>(a, op_s, blockIdx.x, gridDim.x);
 }
 
@@ -86,7 +97,7 @@ __global__ void __launch_bounds__(kResidentThreads) sddmm_resident(const SddmmAr
   extern __shared__ __align__(128) float op_s[];
   __shared__ uint64_t bar;
   griddep_wait();
-  stage_operand(a.xt, n_op * BW, op_s, &bar, err);
+  if (!stage_operand(a.xt, n_op * BW, op_s, &bar, err)) return;
   sddmm_part<BW, LPS, true>(a, op_s, blockIdx.x, gridDim.x);
 }
 
@@ -126,7 +137,33 @@ cudaError_t launch_resident(K kern, const A &a, int64_t n_op, int *err, size_t s
   return cudaLaunchKernelEx(&cfg, kern, a, n_op, err);
 }
 
+// Self-test of the failure path: an mbarrier that expects 16 bytes nobody
+// sends, waited on with a short bound; the block records the time-out in
+// *err and exits normally.
+__global__ void __launch_bounds__(32) wait_selftest(int *err, uint32_t limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&bar)), "r"(1) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&bar)),
+                 "r"(16u)
+                 : "memory");
+  const bool ok = __syncthreads_and(mbar_wait(&bar, 0, limit));
+  if (threadIdx.x == 0) {
+    if (!ok) atomicOr(err, 1);
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(&bar)) : "memory");
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(int *err, cudaStream_t s) {
+  wait_selftest<<<1, 32, 0, s>>>(err, 1024u);
+  return cudaGetLastError();
+}
 
 // Slices of 1-4 floats whose whole operand fits in 192 KB, on layers of at
 // least 2^22 entries whose value bytes cover the staging copies (one operand

@@ -152,6 +152,9 @@ cudaError_t launch_backward_fused(const Plan &pc, const SpmmArgs &cols, const Pl
 bool resident_fits(int bw, int64_t n_op, int64_t nseg, int64_t nnz);
 cudaError_t launch_resident_spmm(bool perm, const Plan &p, const SpmmArgs &a, int64_t n_op,
                                  int *err, bool pdl, cudaStream_t s);
+// One block that waits, with a short bound, on an mbarrier nothing completes
+// and sets *err when it gives up (the failure path of the bounded waits).
+cudaError_t launch_wait_selftest(int *err, cudaStream_t s);
 cudaError_t launch_resident_sddmm(const Plan &p, const SddmmArgs &a, int64_t n_op, int *err,
                                   bool pdl, cudaStream_t s);
 // at[c * bw + b] = a[b * a_ld + c] and bt likewise, in one launch.

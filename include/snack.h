@@ -296,6 +296,17 @@ snack_status snack_forward_csr_static(int64_t out_features, int64_t in_features,
 snack_status snack_device_error(snack_handle h, int *flag, void *stream);
 
 /*
+ * Self-test of that failure path: one block waits, with a short bound, on a
+ * device barrier that nothing completes, and records the time-out the way
+ * the kernels record a failed wait.  *timed_out receives 1 when the wait
+ * gave up as designed; the context stays usable afterwards.  The paper has
+ * no counterpart to this call; it exists to test the bounded waits without
+ * faulting or hanging the GPU.  Allocates a device int; synchronises
+ * `stream`.  Errors report through snack_last_error(NULL).
+ */
+snack_status snack_selftest_wait(void *stream, int *timed_out);
+
+/*
  * Kernel launches this library has issued in the process so far (all
  * handles, all threads).  Launches recorded into a CUDA graph count once,
  * at capture.  For accounting and tests.

@@ -427,3 +427,16 @@ def test_prune_regrow_large_layer():
     assert (p, t) == (o["pruned"], o["trials"])
     assert p == math.floor(float(np.float32(0.3)) * L.nnz)
     check_topology(h, canonical(L.out, L.inp, o["row"], o["col"], o["val"]))
+
+
+# ------------------------------------------------------------ failure path
+
+def test_bounded_wait_gives_up_and_context_stays_usable():
+    # a device barrier that nothing completes: the bounded wait gives up,
+    # records it and returns; the GPU keeps working
+    m = sn()
+    assert m.snack_selftest_wait() == 1
+    L = workloads.workload("toy256").layers[0]
+    row, col, val = L.coo()
+    h, ref = _layer_case(L.out, L.inp, row, col, val, [4], seed=9)
+    assert m.snack_device_error(h) == 0
