@@ -49,12 +49,11 @@ inline int64_t resident_capacity(K kern) {
 // kernel on the stream is still running; the kernel's griddep_wait() holds
 // it until that kernel has completed and its writes are visible.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_ex(void (*kern)(KArgs...), int64_t grid, bool pdl, cudaStream_t s,
+inline cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, bool pdl, cudaStream_t s,
                              Args &&...args) {
-  if (grid < 1) return cudaSuccess;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if (grid.x < 1 || grid.y < 1) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
@@ -64,6 +63,14 @@ inline cudaError_t launch_ex(void (*kern)(KArgs...), int64_t grid, bool pdl, cud
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kern)(KArgs...), int64_t grid, bool pdl, cudaStream_t s,
+                             Args &&...args) {
+  if (grid < 1) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  return launch_ex(kern, dim3((unsigned)grid), pdl, s, std::forward<Args>(args)...);
 }
 
 // Team sizes are compiled for 8, 16 and 32 lanes.
@@ -107,21 +114,34 @@ constexpr int half_team(int W, int L) {
 inline int64_t teams_of(const SpmmArgs &a) { return a.nseg * a.nsub; }
 inline int64_t teams_of(const SddmmArgs &a) { return a.nseg * a.nsub; }
 
+// Grid rows: SpMM batch sub-slices run as gridDim.y (the segment loop then
+// stays the same); the SDDMM's entry sub-ranges are part of its team index.
+inline int grid_rows(const SpmmArgs &a) { return a.nsub; }
+inline int grid_rows(const SddmmArgs &) { return 1; }
+
+// Persistent grid of `cap` resident blocks for `teams` teams of L lanes,
+// `rows` grid rows sharing them.
+inline dim3 one_wave_grid(int64_t teams, int L, int64_t cap, int rows) {
+  const int64_t per_row = (teams / rows * L + 255) / 256;
+  int64_t cap_row = cap / rows;
+  if (cap_row < 1) cap_row = 1;
+  return dim3((unsigned)(per_row < cap_row ? per_row : cap_row), (unsigned)rows);
+}
+
 template <typename K, typename KH, typename A>
 inline cudaError_t launch_one_wave(K k, int L, KH kh, int LH, A a, bool pdl, cudaStream_t s) {
   const int64_t cap = resident_capacity(k);
   const int64_t teams = teams_of(a);
+  const int rows = grid_rows(a);
   if (LH < L) {
     const int64_t cap_h = resident_capacity(kh);
     if (teams > cap * (256 / L) && teams <= cap_h * (256 / LH)) {
       a.lps = LH;
-      const int64_t need = (teams * LH + 255) / 256;
-      return launch_ex(kh, need < cap_h ? need : cap_h, pdl, s, a);
+      return launch_ex(kh, one_wave_grid(teams, LH, cap_h, rows), pdl, s, a);
     }
   }
   a.lps = L;
-  const int64_t need = (teams * L + 255) / 256;
-  return launch_ex(k, need < cap ? need : cap, pdl, s, a);
+  return launch_ex(k, one_wave_grid(teams, L, cap, rows), pdl, s, a);
 }
 
 // CALL2(W, L) for the slice width and team size of a plan.

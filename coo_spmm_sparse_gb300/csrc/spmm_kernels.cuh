@@ -331,20 +331,20 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
   const int64_t stride = nblocks * teams_per_block;
   const int64_t my_team = block * teams_per_block + threadIdx.x / lps;
   const int64_t warp_team = block * teams_per_block + (threadIdx.x & ~31) / lps;
-  // Batch sub-slices (nsub > 1, lines never split): team t works on segment
-  // t % nseg for the BW-wide sub-slice t / nseg of an operand whose rows are
-  // a.stride floats apart.
+  // Batch sub-slice of this block (blockIdx.y, 0 unless the launch cuts the
+  // slice into sub-slices; tables with split lines never are): columns
+  // part_b * BW .. of an operand whose rows are a.stride floats apart.
+  const int part_b = blockIdx.y;
   const int ld = SM ? BW : a.stride;
-  const int64_t nteams = a.nseg * a.nsub;
+  const float *src = op + part_b * BW + sub * VEC;
+  float *const dst = a.dst + (int64_t)part_b * BW * a.ld;
+  const int nb = a.nb - part_b * BW;
 
-  for (int64_t t0 = 0; warp_team + t0 < nteams; t0 += stride) {
+  for (int64_t t0 = 0; warp_team + t0 < a.nseg; t0 += stride) {
     const int64_t team = my_team + t0;
-    const bool active = team < nteams;
-    const int part_b = a.nsub > 1 && active ? (int)(team / a.nseg) : 0;
-    const int64_t segi = team - (int64_t)part_b * a.nseg;
-    const float *src = op + part_b * BW + sub * VEC;
+    const bool active = team < a.nseg;
     int4 sg = make_int4(0, 0, 0, -1);
-    if (active) sg = a.seg[segi];
+    if (active) sg = a.seg[team];
     const int k0 = sg.y, k1 = sg.z;
 
     float acc[NV][VEC];
@@ -394,15 +394,13 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
     if (!active) continue;
     const int line = sg.x;
     if (sg.w < 0) {
-      if (grp == 0)
-        store_line<BW>(a.dst + (int64_t)part_b * BW * a.ld, a.ld, a.nb - part_b * BW, line, sub,
-                       acc);
+      if (grp == 0) store_line<BW>(dst, a.ld, nb, line, sub, acc);
       continue;
     }
 
     // Line split over several segments: park the partial, last arrival sums.
     const int4 sp = a.split[sg.w];  // {first segment, parts, first slot, 0}
-    const int part = (int)(segi - sp.x);
+    const int part = (int)(team - sp.x);
     if (grp == 0) {
       float *mine = a.partial + (int64_t)(sp.z + part) * BW + sub * VEC;
 #pragma unroll
@@ -431,7 +429,7 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
 #pragma unroll
           for (int i = 0; i < VEC; ++i) tot[v][i] += __ldcg(q + v * G * VEC + i);
       }
-      store_line<BW>(a.dst, a.ld, a.nb, line, sub, tot);
+      store_line<BW>(dst, a.ld, nb, line, sub, tot);
     }
     if (tlane == 0) a.counter[sg.w] = 0;  // re-arm for the next call
   }
