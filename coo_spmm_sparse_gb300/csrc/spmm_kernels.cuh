@@ -272,14 +272,14 @@ __device__ __forceinline__ void load_step(const SpmmArgs &a, int kb, int k1, int
 }
 
 // The entries of one group in steps of two quads, gathering the operand
-// from global memory, for canonical-order streams (rows).  The stream loads
-// run one step ahead: while this step's operand rows are gathered, the next
-// step's indices and values are in flight.  A quad past the segment end is
+// from global (SM = false) or shared memory, for canonical-order streams
+// (rows).  The stream loads run one step ahead: while this step's operand
+// rows are gathered, the next step's indices and values are in flight.  A quad past the segment end is
 // not loaded and all its entries are masked.  (The column direction reads
 // its values through the permutation, a load that depends on another; run
 // ahead the same way it measured slower at 64-wide slices, so it keeps the
 // plain loop.)
-template <int BW>
+template <int BW, bool SM>
 __device__ __forceinline__ void walk_pipelined(const SpmmArgs &a, const float *src, int ld, int kb,
                                                int k0, int k1, int npt,
                                                float (&acc)[SliceShape<BW>::NV]
@@ -299,7 +299,7 @@ __device__ __forceinline__ void walk_pipelined(const SpmmArgs &a, const float *s
     int cn[2][4] = {};
     float wn[2][4] = {};
     load_step(a, kb + 8 * npt, k1, npt, cn, wn);
-    gather_fma<BW, 2, false>(src, ld, c, w, ok, acc);
+    gather_fma<BW, 2, SM>(src, ld, c, w, ok, acc);
 #pragma unroll
     for (int q = 0; q < 2; ++q)
 #pragma unroll
@@ -313,7 +313,7 @@ __device__ __forceinline__ void walk_pipelined(const SpmmArgs &a, const float *s
 // Segmented SpMM over blocks [block, ...) of a persistent grid of `nblocks`.
 // PERM = values reached through a column-order -> canonical permutation
 // (the dX = dY W direction while the column-ordered value copy is stale).
-// PIPE = with global gathers and no permutation, run the stream one step
+// PIPE = without a permutation, run the stream one step
 // ahead (walk_pipelined).
 template <int BW, int LPS, bool PERM, bool SM = false, bool PIPE = true>
 __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, int64_t block,
@@ -354,8 +354,8 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
       for (int i = 0; i < VEC; ++i) acc[v][i] = 0.f;
 
     int kb = (k0 & ~3) + 4 * grp;
-    if constexpr (!SM && !PERM && PIPE) {
-      walk_pipelined<BW>(a, src, ld, kb, k0, k1, npt, acc);
+    if constexpr (!PERM && PIPE) {
+      walk_pipelined<BW, SM>(a, src, ld, kb, k0, k1, npt, acc);
     } else {
       for (; kb + 4 * npt < k1; kb += 8 * npt) {  // two quads in flight
         int c[2][4];
