@@ -654,28 +654,22 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, 
 #pragma unroll
       for (int v = 0; v < NV; ++v) load_vec<VEC>(p + v * G * VEC, dy[v]);
     }
-    // Gathering from global memory, the column loads run one step ahead of
-    // the gathers (as in walk_pipelined); from shared memory they do not.
-    // Two quads per step, one with the optimizer step (its operands take the
-    // registers of the second quad).
+    // The column loads run one step ahead of the gathers (as in
+    // walk_pipelined).  Two quads per step, one with the optimizer step (its
+    // operands take the registers of the second quad).
     constexpr int QPS = OPT ? 1 : 2;
     int kb = (k0 & ~3) + 4 * grp;
     int c[2][4] = {};
-    if (!SM) load_col_step<QPS>(a.col, kb, k1, npt, c);
+    load_col_step<QPS>(a.col, kb, k1, npt, c);
     for (; kb < k1; kb += 4 * QPS * npt) {
       int cn[2][4] = {};
-      if (SM)
-        load_col_step<QPS>(a.col, kb, k1, npt, c);
-      else
-        load_col_step<QPS>(a.col, kb + 4 * QPS * npt, k1, npt, cn);
+      load_col_step<QPS>(a.col, kb + 4 * QPS * npt, k1, npt, cn);
       sddmm_quads<BW, SM, OPT>(a, xt, kb, k0, k1, npt, gmask, sub, dy, c,
                                QPS == 2 && kb + 4 * npt < k1);
-      if (!SM) {
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
+      for (int q = 0; q < 2; ++q)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) c[q][e] = cn[q][e];
-      }
+        for (int e = 0; e < 4; ++e) c[q][e] = cn[q][e];
     }
   }
 }
