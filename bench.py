@@ -21,7 +21,7 @@ duration against the measured HBM copy bandwidth), an end-to-end number
 through the same calls with host buffers (one pinned H2D copy of every X and
 dY, one D2H copy of every Y, dX and dW, inside the timed region), the CPU oracle on the host cores on a
 bounded sample, the SM clocks sampled during the timed region, and the
-kernel launches.  The per-op table also times the fused Adam step
+kernel launches.  The per-op table also times the Adam step
 (snack_adam_step) of each layer and batch; it is not part of the metric.
 
 `--impl reference` times the CPU oracle instead (the deliberately slow
@@ -303,7 +303,7 @@ def run_ours(args):
             sn.snack_backward_input(c["h"], d["dY"], d["dX"], stream=stream)
         elif op == "bwd_weight":
             sn.snack_backward_weight(c["h"], d["X"], d["dY"], d["dW"], stream=stream)
-        else:  # fused Adam step (the gradient is not written); not part of the metric
+        else:  # Adam step (gradient + update); not part of the metric
             sn.snack_adam_step(c["h"], d["X"], d["dY"], lr=1e-3, step=1, stream=stream)
 
     with torch.cuda.stream(stream):

@@ -242,8 +242,9 @@ def _opt_inputs(h: SnackHandle, X: torch.Tensor, dY: torch.Tensor):
 
 def snack_sgd_step(h: SnackHandle, X: torch.Tensor, dY: torch.Tensor, lr: float,
                    momentum: float = 0.0, weight_decay: float = 0.0, stream=None) -> None:
-    """One SGD step on the stored values, fused with their gradient
-    sum_b dY[b,row_k] X[b,col_k] (which is not materialised)."""
+    """One SGD step on the stored values from their gradient
+    sum_b dY[b,row_k] X[b,col_k] (never returned; batches of 1-4 compute it
+    inside the step's kernel, larger ones in the handle's gradient buffer)."""
     X, dY, B = _opt_inputs(h, X, dY)
     _check(_lib.snack_sgd_step(h.ptr, _ptr(X), _ptr(dY), B, lr, momentum, weight_decay,
                                _stream(stream, X.device)), h)
@@ -252,8 +253,8 @@ def snack_sgd_step(h: SnackHandle, X: torch.Tensor, dY: torch.Tensor, lr: float,
 def snack_adam_step(h: SnackHandle, X: torch.Tensor, dY: torch.Tensor, lr: float = 1e-3,
                     betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0,
                     step: int = 1, stream=None) -> None:
-    """One Adam step (step = t >= 1) on the stored values, fused with their
-    gradient."""
+    """One Adam step (step = t >= 1) on the stored values from their
+    gradient (as for snack_sgd_step)."""
     X, dY, B = _opt_inputs(h, X, dY)
     _check(_lib.snack_adam_step(h.ptr, _ptr(X), _ptr(dY), B, lr, betas[0], betas[1], eps,
                                 weight_decay, step, _stream(stream, X.device)), h)

@@ -307,40 +307,45 @@ snack_status ensure_opt_state(snack_handle h, int kind, int arrays, cudaStream_t
   return SNACK_OK;
 }
 
-// The fused optimizer step over batch slices of at most 64 (wider slices
-// measured slower: one lane of a group of 16 or 32 carries the update):
-// every slice but the last adds its weight product into the handle's
-// gradient buffer; the last adds that buffer to its own product and applies
-// the step.
-constexpr int64_t kStepSlice = 64;
+// One optimizer step.  Batches of 1-4 (slices of 1-4 floats): one launch of
+// the SDDMM with the step fused in, each entry's gradient updating its value
+// and state in place.  Wider: the plain SDDMM (two quads per step, slices of
+// up to 256, later slices accumulating) writes the whole batch's gradient
+// into the handle's gradient buffer, then a streaming kernel applies the
+// step; the fused kernel's one quad per step halves its gathers in flight,
+// which at 8+ floats per gathered row costs more than the gradient's round
+// trip through memory (10000x10000 @95% Adam at batch 16: 97 -> 58 us).
+constexpr int kFusedStepMaxWidth = 4;
 
 snack_status run_opt_step(snack_handle h, const float *X, const float *dY, int64_t batch,
                           snack::OptArgs o, cudaStream_t s) {
   snack::Layer &L = h->L;
   if (L.nnz == 0) return SNACK_OK;
-  const bool sliced = batch > kStepSlice;
-  if (sliced && !L.d_gacc) {
-    size_t acct = 0;
-    cudaError_t e = snack::dev_alloc(&L.d_gacc, (size_t)L.nnz_pad, &acct);
-    if (e != cudaSuccess) return cuda_fail(h, e, "gradient buffer allocation");
-    account(L);
-  }
   o.val = L.d_val;
   o.s0 = L.d_opt[0];
   o.s1 = o.kind == snack::kOptAdam ? L.d_opt[1] : nullptr;
   if (o.kind == snack::kOptSgd && o.mom == 0.f) o.s0 = nullptr;
   snack_status st;
-  for (int64_t b0 = 0; b0 < batch; b0 += kStepSlice) {
-    const int nb = (int)std::min<int64_t>(kStepSlice, batch - b0);
-    if (b0 + nb < batch) {
-      st = run_backward_slice(h, X, dY, nullptr, L.d_gacc, b0, nb, s);
-    } else {
-      snack::OptArgs last = o;
-      last.gacc = sliced ? L.d_gacc : nullptr;
-      st = run_backward_slice(h, X, dY, nullptr, nullptr, b0, nb, s, &last);
+  const int nb0 = (int)std::min<int64_t>(batch, snack::kMaxSlice);
+  if (snack::choose_plan(L.csr, nb0).bw <= kFusedStepMaxWidth) {
+    st = run_backward_slice(h, X, dY, nullptr, nullptr, 0, nb0, s, &o);
+  } else {
+    if (!L.d_gacc) {
+      size_t acct = 0;
+      cudaError_t e = snack::dev_alloc(&L.d_gacc, (size_t)L.nnz_pad, &acct);
+      if (e != cudaSuccess) return cuda_fail(h, e, "gradient buffer allocation");
+      account(L);
     }
-    if (st != SNACK_OK) return st;
+    for (int64_t b0 = 0; b0 < batch; b0 += snack::kMaxSlice) {
+      const int nb = (int)std::min<int64_t>(snack::kMaxSlice, batch - b0);
+      if ((st = run_backward_slice(h, X, dY, nullptr, L.d_gacc, b0, nb, s)) != SNACK_OK) return st;
+    }
+    cudaError_t e = snack::launch_opt_apply(o, L.d_gacc, L.nnz, true, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "optimizer step launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    st = SNACK_OK;
   }
+  if (st != SNACK_OK) return st;
   // The values changed: the column-ordered copy is stale (dX reads through
   // the permutation) until snack_values_changed() re-derives it.  Keeping it
   // current inside the step (a scattered 4-byte store per entry) measured

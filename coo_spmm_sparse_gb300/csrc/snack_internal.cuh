@@ -69,7 +69,7 @@ struct Layer {
   // optimizer (allocated by the first fused step that needs them)
   int opt_kind = kOptNone;     // kind the state below belongs to
   float *d_opt[2] = {nullptr, nullptr};  // [nnz_pad] momentum / first moment, second moment
-  float *d_gacc = nullptr;     // [nnz_pad] gradient of earlier slices (batches above 64)
+  float *d_gacc = nullptr;     // [nnz_pad] whole-batch gradient of the unfused steps (batch > 4)
   size_t device_bytes = 0;
   std::string last_error;
 };
@@ -107,7 +107,6 @@ struct OptArgs {
   float *val = nullptr;                           // [nnz] values, canonical order
   float *s0 = nullptr;                            // momentum buffer / first moment (or null)
   float *s1 = nullptr;                            // second moment (Adam)
-  const float *gacc = nullptr;                    // gradient of earlier batch slices (or null)
 };
 
 struct SddmmArgs {
@@ -144,6 +143,8 @@ cudaError_t launch_spmm_cols(const Plan &p, const SpmmArgs &a, bool pdl, cudaStr
 cudaError_t launch_sddmm(const Plan &p, const SddmmArgs &a, bool pdl, cudaStream_t s);
 // The same with the optimizer step of a.opt applied instead of writing dW.
 cudaError_t launch_sddmm_step(const Plan &p, const SddmmArgs &a, bool pdl, cudaStream_t s);
+cudaError_t launch_opt_apply(const OptArgs &o, const float *g, int64_t nnz, bool pdl,
+                             cudaStream_t s);
 cudaError_t launch_backward_fused(const Plan &pc, const SpmmArgs &cols, const Plan &pr,
                                   const SddmmArgs &rows, bool pdl, cudaStream_t s);
 // Variants with the whole operand resident in shared memory (slices of 1-4

@@ -461,11 +461,11 @@ __device__ __forceinline__ void store4(float *p, unsigned mask, const float (&x)
 }
 
 // Operands of the optimizer step for one quad (entries whose bit is set in
-// mask): values, state, and the gradient of earlier batch slices.  Loaded
-// before the quad's gathers so that their latency overlaps them.
+// mask): values and state.  Loaded before the quad's gathers so that their
+// latency overlaps them.
 struct OptQuad {
   unsigned mask;
-  float w[4], s0[4], s1[4], ga[4];
+  float w[4], s0[4], s1[4];
 };
 
 __device__ __forceinline__ unsigned quad_mask(int kq, int k0, int k1) {
@@ -481,23 +481,16 @@ __device__ __forceinline__ void opt_load(const OptArgs &o, int kq, unsigned mask
   load4(o.val + kq, mask, q.w);
   if (o.s0) load4(o.s0 + kq, mask, q.s0);
   if (o.s1) load4(o.s1 + kq, mask, q.s1);
-  if (o.gacc) {
-    load4(o.gacc + kq, mask, q.ga);
-  } else {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) q.ga[e] = 0.f;
-  }
 }
 
-// Optimizer step for one quad given this batch slice's gradients res (plus
-// earlier slices' in q.ga).  SGD: d = g + wd w, buf = mom buf + d (with a
+// Optimizer step for one quad given its batch gradients res.  SGD: d = g + wd w, buf = mom buf + d (with a
 // buffer), w -= lr d.  Adam: m = b1 m + (1-b1) d, v = b2 v + (1-b2) d^2,
 // w -= step m / (sqrt(v) / sqrt(1 - b2^t) + eps).
 __device__ __forceinline__ void opt_store(const OptArgs &o, int kq, OptQuad &q,
                                           const float (&res)[4]) {
   float d[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) d[e] = fmaf(o.wd, q.w[e], res[e] + q.ga[e]);
+  for (int e = 0; e < 4; ++e) d[e] = fmaf(o.wd, q.w[e], res[e]);
   if (o.kind == kOptSgd) {
     if (o.s0) {
 #pragma unroll

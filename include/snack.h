@@ -35,8 +35,7 @@
  *     the handle as it was.
  *   - Limits: 1 <= out_features, in_features < 2^31; 0 <= nnz < 2^31 and
  *     nnz <= out_features * in_features; batch >= 1 (any size: batches above
- *     256 run as consecutive slices of 256; the fused optimizer steps use
- *     slices of 64).
+ *     256 run as consecutive slices of 256).
  */
 #ifndef SNACK_H
 #define SNACK_H
@@ -130,7 +129,7 @@ snack_status snack_backward(snack_handle h, const float *X, const float *dY, flo
                             float *dW, int64_t batch, void *stream);
 
 /*
- * One optimizer step on the stored entries, fused with the weight gradient.
+ * One optimizer step on the stored entries from the weight gradient.
  * §3.4: the gradient exists only at supp(W), so only the nnz stored values
  * are trained (frozen cells see no gradient); §4.1 trains with SGD and
  * Appendix G with Adam.  For every stored entry k, with
@@ -153,7 +152,9 @@ snack_status snack_backward(snack_handle h, const float *X, const float *dY, flo
  * (snack_optimizer_state).  The first step that needs them allocates and
  * zeroes them (that call allocates device memory, so make it outside graph
  * capture); a step of the other optimizer kind zeroes them first.  Batches
- * above 64 also use an nnz-long gradient buffer, allocated on first use.
+ * of 1-4 compute the gradient and the step in one kernel; larger batches
+ * write the gradient into an nnz-long buffer of the handle (allocated on
+ * first use, same capture rule) and apply the step in a second kernel.
  * snack_prune_regrow keeps each surviving entry's state and starts regrown
  * entries from zero.  Errors: SNACK_ERR_INVALID_ARG for non-finite lr /
  * weight_decay, momentum < 0, betas outside [0, 1), eps <= 0, step < 1,

@@ -1,5 +1,6 @@
-"""GPU parity of the fused optimizer step (SGD / Adam on the stored entries,
-with the weight gradient computed in the same kernel and never written).
+"""GPU parity of the optimizer step (SGD / Adam on the stored entries; the
+weight gradient is computed inside the step's kernel for batches of 1-4 and
+through the handle's gradient buffer for larger ones, both covered here).
 
 Each step is checked on its own against the oracle: the oracle takes the
 GPU's values and state before the step (read back) and the float64 gradient
@@ -67,7 +68,7 @@ class Case:
         return sn().snack_export(self.h)[2]
 
     def check_dx(self, B):
-        # after fused steps dX reads the values through the column permutation
+        # after optimizer steps dX reads the values through the column permutation
         # (their column-ordered copy is stale); after snack_values_changed()
         # it streams the re-derived copy
         dY = self.g.standard_normal((B, self.out)).astype(np.float32)

@@ -1,5 +1,5 @@
 """The GPT-2-shaped decoder workload trained through the library: every step
-runs the forward, the input gradient and a fused Adam step of each sparse
+runs the forward, the input gradient and an Adam step of each sparse
 layer of one block; every 100 steps each layer is magnitude-pruned by 30 %
 and regrown uniformly (Appendix G's schedule with the workload's fraction).
 
