@@ -68,3 +68,49 @@ def test_decoder_block_training_with_prune_regrow():
         dY = g.standard_normal((16, L.out)).astype(np.float32)
         check_products(h, L.out, L.inp, ref, X, dY)
         assert m.snack_device_error(h) == 0
+
+
+def test_decoder_block_sgd_training_with_prune_regrow():
+    """The decoder workload's own recipe on its second block: plain SGD (no
+    momentum, §4.2) at the workload's learning rate, 300 steps of 256 tokens,
+    30 % magnitude prune / uniform regrow every 100 steps (three topology
+    changes, each bit-exact against the oracle from the trained values)."""
+    m = sn()
+    wl = workloads.workload("gpt2_decoder")
+    frac, lr, every = wl.extra["prune_frac"], wl.extra["lr"], wl.extra["prune_every"]
+    layers = wl.layers[4:8]
+    hs = []
+    for L in layers:
+        row, col, val = L.coo()
+        hs.append(m.snack_create(L.out, L.inp, row, col, val))
+    gen = torch.Generator(device=dev()).manual_seed(9)
+    tokens = wl.extra["ctx"]
+    events = 0
+    for step in range(1, 301):
+        for L, h in zip(layers, hs):
+            X = torch.randn(tokens, L.inp, device=dev(), generator=gen)
+            dY = torch.randn(tokens, L.out, device=dev(), generator=gen) * 1e-2
+            m.snack_forward(h, X)
+            m.snack_backward_input(h, dY)
+            m.snack_sgd_step(h, X, dY, lr=lr)
+        if step % every:
+            continue
+        events += 1
+        for L, h in zip(layers, hs):
+            torch.cuda.synchronize()
+            r0, c0, v0 = m.snack_export(h)
+            seed = 1000 * step + L.seed
+            pruned, trials = m.snack_prune_regrow(h, frac, seed)
+            o = oracle.prune_regrow(L.out, L.inp, r0, c0, v0, frac, seed)
+            assert (pruned, trials) == (o["pruned"], o["trials"])
+            check_topology(h, canonical(L.out, L.inp, o["row"], o["col"], o["val"]))
+            assert h.nnz == L.nnz
+    assert events == 3
+    g = np.random.default_rng(10)
+    for L, h in zip(layers, hs):
+        r, c, v = m.snack_export(h)
+        ref = canonical(L.out, L.inp, r, c, v)
+        X = g.standard_normal((8, L.inp)).astype(np.float32)
+        dY = g.standard_normal((8, L.out)).astype(np.float32)
+        check_products(h, L.out, L.inp, ref, X, dY)
+        assert m.snack_device_error(h) == 0
