@@ -416,21 +416,29 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
     last = __shfl_sync(tmask, last, lane - tlane);
     if (!last) continue;
     __threadfence();
-    if (grp == 0) {
-      float tot[NV][VEC];
+    // The team's npt groups each sum the parts grp, grp + npt, ... in order,
+    // then meet by shuffle: a fixed order for a given plan (reproducible),
+    // with up to npt parts' loads in flight at once.
+    float tot[NV][VEC];
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) tot[v][i] = 0.f;
+#pragma unroll 1
+    for (int p = grp; p < sp.y; p += npt) {
+      const float *q = a.partial + (int64_t)(sp.z + p) * BW + sub * VEC;
 #pragma unroll
       for (int v = 0; v < NV; ++v)
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) tot[v][i] = 0.f;
-      for (int p = 0; p < sp.y; ++p) {
-        const float *q = a.partial + (int64_t)(sp.z + p) * BW + sub * VEC;
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-#pragma unroll
-          for (int i = 0; i < VEC; ++i) tot[v][i] += __ldcg(q + v * G * VEC + i);
-      }
-      store_line<BW>(dst, a.ld, nb, line, sub, tot);
+        for (int i = 0; i < VEC; ++i) tot[v][i] += __ldcg(q + v * G * VEC + i);
     }
+#pragma unroll
+    for (int off = G; off < lps; off <<= 1)
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) tot[v][i] += __shfl_xor_sync(tmask, tot[v][i], off);
+    if (grp == 0) store_line<BW>(dst, a.ld, nb, line, sub, tot);
     if (tlane == 0) a.counter[sg.w] = 0;  // re-arm for the next call
   }
 }
