@@ -34,6 +34,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -190,13 +191,20 @@ def read_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(csrc: str | None = None) -> str:
+    """Hash of the CUDA sources' code: comments and whitespace are removed
+    first, so that an edit to a comment keeps recorded counters valid while
+    any change to the code itself does not."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "coo_spmm_sparse_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "coo_spmm_sparse_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                code = f.read()
+            code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
+            code = re.sub(r"//[^\n]*", " ", code)
+            code = " ".join(code.split())
+            h.update(name.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 

@@ -34,7 +34,7 @@
 namespace snack {
 
 constexpr int kMaxSlice = 256;  // widest batch slice one kernel launch handles
-constexpr int kOptNone = 0, kOptSgd = 1, kOptAdam = 2;  // fused optimizer kinds
+constexpr int kOptNone = 0, kOptSgd = 1, kOptAdam = 2;  // optimizer kinds
 
 struct SegTable {
   int64_t nseg = 0;
@@ -66,7 +66,7 @@ struct Layer {
   float *d_dyt = nullptr;      // [out][kMaxSlice]  transposed dY slice
   float *d_partial = nullptr;  // [max(csr.nslots, csc.nslots)][kMaxSlice]
   int *d_counter = nullptr;    // [max(csr.nsplit, csc.nsplit)], zero between calls
-  // optimizer (allocated by the first fused step that needs them)
+  // optimizer (allocated by the first step that needs them)
   int opt_kind = kOptNone;     // kind the state below belongs to
   float *d_opt[2] = {nullptr, nullptr};  // [nnz_pad] momentum / first moment, second moment
   float *d_gacc = nullptr;     // [nnz_pad] whole-batch gradient of the unfused steps (batch > 4)
@@ -120,7 +120,7 @@ struct SddmmArgs {
   int lps;           // lanes per segment team (set by the launcher)
   int prefetch;      // pull the segments' column streams into L2 while waiting on a transpose
   int nsub;          // entry sub-ranges per segment, one team each
-  OptArgs opt;       // fused optimizer step instead of writing dw
+  OptArgs opt;       // optimizer step fused in instead of writing dw (slices of 1-4)
 };
 
 // Kernel selection: batch slice width, lanes per entry group, lanes per segment.

@@ -203,8 +203,8 @@ snack_status snack_prune_regrow(snack_handle h, float prune_frac, uint64_t seed,
  * The handle also keeps the values in column order, so that dX streams them
  * instead of reading each through the column permutation (creation and
  * snack_prune_regrow derive it).  It is trusted only while the values stay
- * as they were when it was derived: handing out this writable pointer, or a
- * fused optimizer step, makes it stale, and dX then reads the values through
+ * as they were when it was derived: handing out this writable pointer, or an
+ * optimizer step (snack_sgd_step / snack_adam_step), makes it stale, and dX then reads the values through
  * the permutation (same results, slower) until snack_values_changed().
  * Layers whose values stay fixed across many backward calls (a frozen layer,
  * repeated evaluation) gain from calling it once.
@@ -214,11 +214,11 @@ snack_status snack_values(snack_handle h, float **dev_val);
 /*
  * Tell the handle that the values will not change for a while (the caller
  * has finished writing them through the snack_values() pointer, or a run of
- * fused optimizer steps is over): re-derives the column-ordered copy
+ * optimizer steps is over): re-derives the column-ordered copy
  * (asynchronous on `stream`, one gather of the values) and lets dX stream
  * it.  The library then assumes the values change only through its own
- * calls until snack_values() is called again; a fused optimizer step makes
- * the copy stale again.  The paper has no counterpart to this call; it
+ * calls until snack_values() is called again; an optimizer step makes the
+ * copy stale again.  The paper has no counterpart to this call; it
  * exists only for the column-ordered copy.
  */
 snack_status snack_values_changed(snack_handle h, void *stream);
