@@ -21,7 +21,12 @@ duration against the measured HBM copy bandwidth), an end-to-end number
 through the same calls with host buffers (one pinned H2D copy of every X and
 dY, one D2H copy of every Y, dX and dW, inside the timed region), the CPU oracle on the host cores on a
 bounded sample, the SM clocks sampled during the timed region, and the
-kernel launches.  The per-op table also times the Adam step
+kernel launches.  The per-op table (each op replayed from its own CUDA graph,
+10 untimed then 50 timed replays, each after an L2 flush; mean and median
+microseconds) gives GFLOP/s, GB/s of the metric's bytes, the fraction of
+the measured copy peak, and gather_gbs: the 4 * B bytes per stored entry of
+operand rows every op gathers (through L1 or shared memory), the bound that
+takes over from HBM as B grows.  It also times the Adam step
 (snack_adam_step) of each layer and batch; it is not part of the metric.
 
 `--impl reference` times the CPU oracle instead (the deliberately slow
@@ -302,7 +307,7 @@ def run_ours(args):
     # own CUDA graph between events on the launching stream, after an L2
     # flush that keeps the GPU busy while the host queues the replay.
     ops = []
-    reps = max(5, min(50, args.steps))
+    reps = 50  # per op: 50 timed replays after 10 untimed ones
 
     def run_op(op, c, d):
         if op == "fwd":
@@ -325,7 +330,8 @@ def run_ours(args):
                     g_op = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(g_op, stream=stream):
                         run_op(op, c, d)
-                    g_op.replay()
+                    for _ in range(10):
+                        g_op.replay()
                     ts = []
                     for _ in range(reps):
                         flush_l2(flush)
@@ -339,13 +345,16 @@ def run_ours(args):
                     if op == "adam_step":  # the steps changed the values: re-derive
                         sn.snack_values_changed(c["h"])  # their column-ordered copy
                         torch.cuda.synchronize()
-                    us = statistics.mean(a.elapsed_time(b) for a, b in ts) * 1e3
+                    durs = [a.elapsed_time(b) * 1e3 for a, b in ts]
+                    us = statistics.mean(durs)
                     nbytes = metric_bytes(op, L.nnz, L.out, L.inp, B)
                     plan_op = {"fwd": 0, "bwd_input": 1}.get(op, 2)  # dW and Adam: rows
                     bw, lanes, segs = sn.snack_plan(c["h"], plan_op, B)
                     ops.append(dict(op=op, layer=L.name, shape=f"{L.out}x{L.inp}", nnz=L.nnz, B=B,
-                                    us=round(us, 3), gflops=round(2 * L.nnz * B / us / 1e3, 2),
+                                    us=round(us, 3), us_median=round(statistics.median(durs), 3),
+                                    gflops=round(2 * L.nnz * B / us / 1e3, 2),
                                     gbs=round(nbytes / us / 1e3, 1), bytes=nbytes,
+                                    gather_gbs=round(4 * B * L.nnz / us / 1e3, 1),
                                     plan=dict(slice=bw, lanes=lanes, segments=segs)))
     peak, peak_kind = read_peak()
     for o in ops:
