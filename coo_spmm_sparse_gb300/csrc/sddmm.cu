@@ -16,8 +16,8 @@ cudaError_t launch_sddmm(const Plan &p, const SddmmArgs &args, bool pdl, cudaStr
 
 cudaError_t launch_transpose(const float *src, int64_t ld, int nb, int64_t ncols, float *dst,
                              int bw, cudaStream_t s, bool pdl) {
-  const int64_t tiles = (ncols + 31) / 32;
-#define SNACK_CALL(W) return launch_ex(transpose_pad<W>, tiles, pdl, s, src, ld, nb, ncols, dst);
+#define SNACK_CALL(W) \
+  return launch_ex(transpose_pad<W>, transpose_tiles<W>(ncols), pdl, s, src, ld, nb, ncols, dst);
   SNACK_BW_SWITCH_WIDE(bw, SNACK_CALL)
 #undef SNACK_CALL
 }
@@ -25,10 +25,9 @@ cudaError_t launch_transpose(const float *src, int64_t ld, int nb, int64_t ncols
 cudaError_t launch_transpose_pair(const float *a, int64_t a_ld, int64_t a_cols, float *at,
                                   const float *b, int64_t b_ld, int64_t b_cols, float *bt, int nb,
                                   int bw, cudaStream_t s, bool pdl) {
-  const int64_t a_tiles = (a_cols + 31) / 32, b_tiles = (b_cols + 31) / 32;
-#define SNACK_CALL(W)                                                                    \
-  return launch_ex(transpose_pair<W>, a_tiles + b_tiles, pdl, s, a, a_ld, a_cols, at, b, \
-                   b_ld, b_cols, bt, nb, a_tiles);
+#define SNACK_CALL(W)                                                                      \
+  return launch_ex(transpose_pair<W>, transpose_tiles<W>(a_cols) + transpose_tiles<W>(b_cols), \
+                   pdl, s, a, a_ld, a_cols, at, b, b_ld, b_cols, bt, nb, transpose_tiles<W>(a_cols));
   SNACK_BW_SWITCH_WIDE(bw, SNACK_CALL)
 #undef SNACK_CALL
 }

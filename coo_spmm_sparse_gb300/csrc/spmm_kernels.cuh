@@ -723,21 +723,37 @@ __global__ void __launch_bounds__(256) backward_segments(const SpmmArgs cols, co
     sddmm_part<BW, LPS>(rows, rows.xt, blockIdx.x - cols_blocks, gridDim.x - cols_blocks);
 }
 
-// dst[c * BW + b] = b < nb ? src[b * ld + c] : 0 for 32 columns per block.
+// Rows of the slice per transpose tile (tiles are 32 columns by this many
+// rows, so that wide slices still spread over many blocks).
+template <int BW>
+__host__ __device__ constexpr int transpose_rows() {
+  return BW < 32 ? BW : 32;
+}
+
+// Tiles of one transpose: 32-column tiles times row tiles.
+template <int BW>
+inline int64_t transpose_tiles(int64_t ncols) {
+  return (ncols + 31) / 32 * (BW / transpose_rows<BW>());
+}
+
+// dst[c * BW + b] = b < nb ? src[b * ld + c] : 0 for one tile of 32 columns
+// by transpose_rows<BW>() rows (the row tile varies fastest with `tile`).
 template <int BW>
 __device__ __forceinline__ void transpose_tile(const float *__restrict__ src, int64_t ld, int nb,
                                                int64_t ncols, float *__restrict__ dst, int64_t tile,
                                                float (*buf)[33]) {
+  constexpr int RT = transpose_rows<BW>(), NRT = BW / RT;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int64_t c0 = tile * 32;
-  for (int b = ty; b < BW; b += 8) {
+  const int64_t c0 = tile / NRT * 32;
+  const int r0 = (int)(tile % NRT) * RT;
+  for (int b = ty; b < RT; b += 8) {
     const int64_t c = c0 + tx;
-    buf[b][tx] = (b < nb && c < ncols) ? src[(int64_t)b * ld + c] : 0.f;
+    buf[b][tx] = (r0 + b < nb && c < ncols) ? src[(int64_t)(r0 + b) * ld + c] : 0.f;
   }
   __syncthreads();
-  for (int f = threadIdx.x; f < 32 * BW; f += 256) {
-    const int cc = f / BW, b = f % BW;
-    if (c0 + cc < ncols) dst[(c0 + cc) * BW + b] = buf[b][cc];
+  for (int f = threadIdx.x; f < 32 * RT; f += 256) {
+    const int cc = f / RT, b = f % RT;
+    if (c0 + cc < ncols) dst[(c0 + cc) * BW + r0 + b] = buf[b][cc];
   }
 }
 
@@ -745,7 +761,7 @@ template <int BW>
 __global__ void __launch_bounds__(256) transpose_pad(const float *__restrict__ src, int64_t ld,
                                                      int nb, int64_t ncols,
                                                      float *__restrict__ dst) {
-  __shared__ float buf[BW][33];
+  __shared__ float buf[transpose_rows<BW>()][33];
   griddep_launch();
   griddep_wait();
   transpose_tile<BW>(src, ld, nb, ncols, dst, blockIdx.x, buf);
@@ -759,7 +775,7 @@ __global__ void __launch_bounds__(256) transpose_pair(const float *__restrict__ 
                                                       const float *__restrict__ b, int64_t b_ld,
                                                       int64_t b_cols, float *__restrict__ bt,
                                                       int nb, int64_t a_tiles) {
-  __shared__ float buf[BW][33];
+  __shared__ float buf[transpose_rows<BW>()][33];
   griddep_launch();
   griddep_wait();
   if ((int64_t)blockIdx.x < a_tiles)
