@@ -117,6 +117,7 @@ snack::SpmmArgs spmm_args(snack::Layer &L, bool rows, const float *op, float *ds
   a.prefetch = 0;
   a.stride = 0;  // set with the plan
   a.nsub = 1;
+  a.stage = (rows ? L.csr.nsplit : L.csc.nsplit) == 0;
   return a;
 }
 

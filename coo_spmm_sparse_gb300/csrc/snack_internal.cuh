@@ -94,6 +94,8 @@ struct SpmmArgs {
   int stride;           // floats between operand rows (the transposed slice's width)
   int nsub;             // batch sub-slices of BW columns, one team per (sub-slice, segment);
                         // > 1 only for tables without split lines
+  int stage;            // table without split lines (segment s is line s): slices of 128+
+                        // with one team per warp write their outputs through shared memory
 };
 
 // Optimizer step fused into the SDDMM epilogue (kind != kOptNone): the

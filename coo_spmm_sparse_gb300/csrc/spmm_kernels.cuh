@@ -340,7 +340,23 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
   float *const dst = a.dst + (int64_t)part_b * BW * a.ld;
   const int nb = a.nb - part_b * BW;
 
-  for (int64_t t0 = 0; warp_team + t0 < a.nseg; t0 += stride) {
+  // Staged output (slices of 128+, one team per warp, no split lines): a
+  // line's outputs are a column of the row-major output, BW scattered
+  // 4-byte stores.  Instead the block's 8 warps, which hold 8 consecutive
+  // lines in every round, park their results in shared memory (double
+  // buffered, rows padded by 4 so the reads below are conflict-free) and the
+  // block writes each output row's 8 consecutive lines as one 32-byte run.
+  // The round count is then the block's, so every warp meets the barrier.
+  // (At 64-wide slices the stores are too small a part of the work to pay
+  // for the barrier: 10000x10000 @95% forward 93.6 -> 95.0 us.)
+  constexpr bool kCanStage = BW >= 128 && LPS == 32 && !SM;
+  constexpr int kStW = kCanStage ? BW + 4 : 1;
+  __shared__ __align__(16) float stage_buf[kCanStage ? 2 : 1][kCanStage ? 8 : 1][kStW];
+  const bool staged = kCanStage && a.stage;
+  const int64_t block_team0 = block * teams_per_block;
+
+  int64_t round = 0;
+  for (int64_t t0 = 0; (staged ? block_team0 : warp_team) + t0 < a.nseg; t0 += stride, ++round) {
     const int64_t team = my_team + t0;
     const bool active = team < a.nseg;
     int4 sg = make_int4(0, 0, 0, -1);
@@ -391,6 +407,25 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
 #pragma unroll
         for (int i = 0; i < VEC; ++i) acc[v][i] += __shfl_xor_sync(0xffffffffu, acc[v][i], off);
 
+    if constexpr (kCanStage) {
+      if (staged) {
+        float(*st)[kStW] = stage_buf[round & 1];
+        const int w = threadIdx.x >> 5;
+        if (grp == 0) {
+#pragma unroll
+          for (int v = 0; v < NV; ++v)
+            *reinterpret_cast<float4 *>(&st[w][v * G * VEC + sub * VEC]) =
+                make_float4(acc[v][0], acc[v][1], acc[v][2], acc[v][3]);
+        }
+        __syncthreads();
+        const int64_t line0 = block_team0 + t0;  // segment s is line s
+        for (int f = threadIdx.x; f < 8 * BW; f += blockDim.x) {
+          const int b = f >> 3, j = f & 7;
+          if (b < nb && line0 + j < a.nseg) dst[(int64_t)b * a.ld + line0 + j] = st[j][b];
+        }
+        continue;
+      }
+    }
     if (!active) continue;
     const int line = sg.x;
     if (sg.w < 0) {
