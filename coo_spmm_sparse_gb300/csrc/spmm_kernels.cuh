@@ -654,7 +654,7 @@ __device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt,
 // grid of `nblocks`; a team's lanes stay together, groups never diverge).
 // OPT: apply the optimizer step of a.opt instead of writing dW (compiled
 // separately, so the plain kernels keep their registers).
-template <int BW, int LPS, bool SM = false, bool OPT = false>
+template <int BW, int LPS, bool SM = false, bool OPT = false, bool FUSED = false>
 __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, int64_t block,
                                            int64_t nblocks) {
   using S = SliceShape<BW>;
@@ -691,9 +691,13 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, 
       for (int v = 0; v < NV; ++v) load_vec<VEC>(p + v * G * VEC, dy[v]);
     }
     // The column loads run one step ahead of the gathers (as in
-    // walk_pipelined).  Two quads per step, one with the optimizer step (its
-    // operands take the registers of the second quad).
-    constexpr int QPS = OPT ? 1 : 2;
+    // walk_pipelined).  Two quads per step; one with the optimizer step (its
+    // operands take the registers of the second quad), and one for rows of
+    // 128+ floats (64+ inside the fused backward), where the second quad's
+    // gathered rows cost resident warps: 96 -> 64 registers, 2 -> 4 blocks
+    // per SM (10000x10000 @95% batch 256 dW 353 -> 343 us, the decoder
+    // workload's fused backward step +7 %; a standalone 64-wide dW lost 5 %).
+    constexpr int QPS = (OPT || BW >= 128 || (FUSED && BW >= 64)) ? 1 : 2;
     int kb = (k0 & ~3) + 4 * grp;
     int c[2][4] = {};
     load_col_step<QPS>(a.col, kb, k1, npt, c);
@@ -755,7 +759,8 @@ __global__ void __launch_bounds__(256) backward_segments(const SpmmArgs cols, co
   if ((int)blockIdx.x < cols_blocks)
     spmm_part<BW, LPS, PERM, false, false>(cols, cols.src, blockIdx.x, cols_blocks);
   else
-    sddmm_part<BW, LPS>(rows, rows.xt, blockIdx.x - cols_blocks, gridDim.x - cols_blocks);
+    sddmm_part<BW, LPS, false, false, true>(rows, rows.xt, blockIdx.x - cols_blocks,
+                                            gridDim.x - cols_blocks);
 }
 
 // Rows of the slice per transpose tile (tiles are 32 columns by this many
