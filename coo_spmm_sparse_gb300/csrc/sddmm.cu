@@ -9,7 +9,7 @@ cudaError_t launch_sddmm(const Plan &p, const SddmmArgs &args, bool pdl, cudaStr
   a.lps = team_lanes(p);
 #define SNACK_CALL(W, L)                                                               \
   return launch_one_wave(sddmm_segments<W, L>, L, sddmm_segments<W, half_team(W, L)>, \
-                         half_team(W, L), a, pdl, s);
+                         half_team(W, L), may_halve(p, half_team(W, L)), a, pdl, s);
   SNACK_BW_LPS_SWITCH(p.bw, a.lps, SNACK_CALL)
 #undef SNACK_CALL
 }
@@ -53,6 +53,7 @@ int device_sms() { return sm_count(); }
 Plan plan_for_width(const SegTable &t, int bw) {
   Plan p;
   p.bw = bw;
+  p.mean_len = t.mean_len;
   const int g = lanes_for(p.bw);
   const double want = t.mean_len / 8.0;
   int npt = 1;

@@ -46,7 +46,7 @@ cudaError_t launch_sddmm_step(const Plan &p, const SddmmArgs &args, bool pdl, cu
   // the gradient buffer with opt_apply).
 #define SNACK_CALL(W, L)                                                                 \
   return launch_one_wave(sddmm_segments<W, L, true>, L, sddmm_segments<W, half_team(W, L), true>, \
-                         half_team(W, L), a, pdl, s);
+                         half_team(W, L), may_halve(p, half_team(W, L)), a, pdl, s);
   switch (p.bw * 64 + a.lps) {
     case 1 * 64 + 8: SNACK_CALL(1, 8)
     case 1 * 64 + 16: SNACK_CALL(1, 16)

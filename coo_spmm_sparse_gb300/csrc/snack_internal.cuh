@@ -129,6 +129,7 @@ struct SddmmArgs {
 struct Plan {
   int bw = 1;
   int lanes = 32;
+  double mean_len = 0.0;  // mean entries per segment of the table planned for
 };
 int slice_width(int64_t nb);
 Plan choose_plan(const SegTable &t, int64_t nb);

@@ -106,11 +106,6 @@ constexpr int half_team(int W, int L) {
   return (L / 2 >= 8 && L / 2 >= lanes_for(W)) ? L / 2 : L;
 }
 
-// Launch `k` (teams of L lanes) on a persistent grid, unless the segments
-// overflow one wave of resident teams by less than what `kh` (teams of LH
-// = half_team lanes) can hold at once: then the last segments would run as
-// a second wave behind their teams' first ones, so `kh` runs instead with
-// every segment resident from the start.
 inline int64_t teams_of(const SpmmArgs &a) { return a.nseg * a.nsub; }
 inline int64_t teams_of(const SddmmArgs &a) { return a.nseg * a.nsub; }
 
@@ -128,12 +123,28 @@ inline dim3 one_wave_grid(int64_t teams, int L, int64_t cap, int rows) {
   return dim3((unsigned)(per_row < cap_row ? per_row : cap_row), (unsigned)rows);
 }
 
+// Whether halving the team may pay: only while a half-size team still walks
+// an average segment in at most four steps (two quads of four entries per
+// group per step).  On long segments the doubled walk costs more than the
+// second wave it avoids (10000x10000 @95% batch 32 forward 66.3 -> 60.2 us
+// without halving), on short ones the halving wins (8192x8192 Zipf-row
+// batch 16 forward 24.5 -> 22.6 us with it).
+inline bool may_halve(const Plan &p, int LH) {
+  return p.mean_len <= 4.0 * 8.0 * LH / lanes_for(p.bw);
+}
+
+// Launch `k` (teams of L lanes) on a persistent grid, unless the segments
+// overflow one wave of resident teams by less than what `kh` (teams of LH
+// = half_team lanes) can hold at once: then the last segments would run as
+// a second wave behind their teams' first ones, so `kh` runs instead with
+// every segment resident from the start (if halve_ok).
 template <typename K, typename KH, typename A>
-inline cudaError_t launch_one_wave(K k, int L, KH kh, int LH, A a, bool pdl, cudaStream_t s) {
+inline cudaError_t launch_one_wave(K k, int L, KH kh, int LH, bool halve_ok, A a, bool pdl,
+                                   cudaStream_t s) {
   const int64_t cap = resident_capacity(k);
   const int64_t teams = teams_of(a);
   const int rows = grid_rows(a);
-  if (LH < L) {
+  if (LH < L && halve_ok) {
     const int64_t cap_h = resident_capacity(kh);
     if (teams > cap * (256 / L) && teams <= cap_h * (256 / LH)) {
       a.lps = LH;
