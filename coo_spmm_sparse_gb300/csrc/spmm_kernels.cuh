@@ -313,8 +313,8 @@ __device__ __forceinline__ void walk_pipelined(const SpmmArgs &a, const float *s
 // Segmented SpMM over blocks [block, ...) of a persistent grid of `nblocks`.
 // PERM = values reached through a column-order -> canonical permutation
 // (the dX = dY W direction while the column-ordered value copy is stale).
-// PIPE = without a permutation, run the stream one step
-// ahead (walk_pipelined).
+// PIPE = without a permutation, run the stream one step ahead
+// (walk_pipelined).  SM = the operand is in shared memory.
 template <int BW, int LPS, bool PERM, bool SM = false, bool PIPE = true>
 __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, int64_t block,
                                           int64_t nblocks) {
