@@ -33,7 +33,7 @@ __all__ = [
     "SnackError", "SnackHandle", "snack_create", "snack_create_random", "snack_forward",
     "snack_backward_input", "snack_backward_weight", "snack_backward", "snack_prune_regrow",
     "snack_values", "snack_values_changed", "snack_sgd_step", "snack_adam_step", "snack_optimizer_state", "snack_export", "snack_export_segments", "snack_plan", "snack_nnz",
-    "snack_device_bytes", "snack_destroy", "snack_launch_count", "snack_forward_csr_static", "snack_device_error", "snack_selftest_wait", "SnackLinear", "library_path",
+    "snack_device_bytes", "snack_destroy", "snack_launch_count", "snack_debug_fail_alloc", "snack_forward_csr_static", "snack_device_error", "snack_selftest_wait", "SnackLinear", "library_path",
 ]
 
 
@@ -338,6 +338,12 @@ def snack_device_error(h: SnackHandle) -> int:
     f = ctypes.c_int(0)
     _check(_lib.snack_device_error(h.ptr, ctypes.byref(f), _stream(None)), h)
     return int(f.value)
+
+
+def snack_debug_fail_alloc(after: int) -> None:
+    """Test hook: after `after` more device allocations by the library, one
+    fails as out of memory (the hook then disarms); negative disarms."""
+    _lib.snack_debug_fail_alloc(int(after))
 
 
 def snack_launch_count() -> int:

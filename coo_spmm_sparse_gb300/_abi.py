@@ -36,6 +36,7 @@ SIGNATURES = {
     "snack_plan": (ctypes.c_int, [vp, ctypes.c_int, i64, P(i32), P(i32), P(i64), P(i32)]),
     "snack_forward_csr_static": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp, vp, i64, vp]),
     "snack_launch_count": (u64, []),
+    "snack_debug_fail_alloc": (None, [i64]),
     "snack_device_error": (ctypes.c_int, [vp, P(ctypes.c_int), vp]),
     "snack_selftest_wait": (ctypes.c_int, [vp, P(ctypes.c_int)]),
     "snack_nnz": (i64, [vp]),

@@ -20,6 +20,7 @@ namespace {
 
 thread_local std::string g_create_error;
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int64_t> g_fail_alloc{-1};  // allocations left before the test hook fires
 
 snack_status fail(snack_handle h, snack_status st, const std::string &msg) {
   if (h)
@@ -285,23 +286,50 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
   return SNACK_OK;
 }
 
-// Optimizer state of the requested kind: allocated (zeroed) on first use;
-// state of another kind is zeroed first.
-snack_status ensure_opt_state(snack_handle h, int kind, int arrays, cudaStream_t s) {
+// Batches of 1-4 (slices of 1-4 floats) take the SDDMM with the optimizer
+// step fused in; wider ones go through the gradient buffer (see run_opt_step).
+constexpr int kFusedStepMaxWidth = 4;
+
+bool step_is_fused(const snack::Layer &L, int64_t batch) {
+  return snack::choose_plan(L.csr, std::min<int64_t>(batch, snack::kMaxSlice)).bw <=
+         kFusedStepMaxWidth;
+}
+
+// Device buffers of an optimizer step, allocated on first use: the gradient
+// buffer (unfused batches) and `arrays` state arrays of `kind` (zeroed; all
+// state is zeroed again when the kind changes).  If an allocation fails,
+// what this call allocated is freed again, so the handle stays as it was.
+snack_status ensure_step_buffers(snack_handle h, int kind, int arrays, int64_t batch,
+                                 cudaStream_t s) {
   snack::Layer &L = h->L;
+  float **made[3];
+  int nmade = 0;
+  auto undo = [&](cudaError_t e, const char *what) {
+    for (int i = 0; i < nmade; ++i) {
+      cudaFree(*made[i]);
+      *made[i] = nullptr;
+    }
+    return cuda_fail(h, e, what);
+  };
   cudaError_t e;
+  size_t acct = 0;
+  if (L.nnz > 0 && !step_is_fused(L, batch) && !L.d_gacc) {
+    if ((e = snack::dev_alloc(&L.d_gacc, (size_t)L.nnz_pad, &acct)) != cudaSuccess)
+      return undo(e, "gradient buffer allocation");
+    made[nmade++] = &L.d_gacc;
+  }
   for (int i = 0; i < arrays; ++i) {
     if (L.d_opt[i]) continue;
-    size_t acct = 0;
     if ((e = snack::dev_alloc(&L.d_opt[i], (size_t)L.nnz_pad, &acct)) != cudaSuccess)
-      return cuda_fail(h, e, "optimizer state allocation");
+      return undo(e, "optimizer state allocation");
+    made[nmade++] = &L.d_opt[i];
     if ((e = cudaMemsetAsync(L.d_opt[i], 0, (size_t)L.nnz_pad * 4, s)) != cudaSuccess)
-      return cuda_fail(h, e, "optimizer state zeroing");
+      return undo(e, "optimizer state zeroing");
   }
-  if (L.opt_kind != kind) {
+  if (arrays > 0 && L.opt_kind != kind) {
     for (float *p : L.d_opt)
       if (p && (e = cudaMemsetAsync(p, 0, (size_t)L.nnz_pad * 4, s)) != cudaSuccess)
-        return cuda_fail(h, e, "optimizer state zeroing");
+        return undo(e, "optimizer state zeroing");
     L.opt_kind = kind;
   }
   account(L);
@@ -316,7 +344,7 @@ snack_status ensure_opt_state(snack_handle h, int kind, int arrays, cudaStream_t
 // step; the fused kernel's one quad per step halves its gathers in flight,
 // which at 8+ floats per gathered row costs more than the gradient's round
 // trip through memory (10000x10000 @95% Adam at batch 16: 97 -> 58 us).
-constexpr int kFusedStepMaxWidth = 4;
+// The buffers are allocated beforehand (ensure_step_buffers).
 
 snack_status run_opt_step(snack_handle h, const float *X, const float *dY, int64_t batch,
                           snack::OptArgs o, cudaStream_t s) {
@@ -327,16 +355,9 @@ snack_status run_opt_step(snack_handle h, const float *X, const float *dY, int64
   o.s1 = o.kind == snack::kOptAdam ? L.d_opt[1] : nullptr;
   if (o.kind == snack::kOptSgd && o.mom == 0.f) o.s0 = nullptr;
   snack_status st;
-  const int nb0 = (int)std::min<int64_t>(batch, snack::kMaxSlice);
-  if (snack::choose_plan(L.csr, nb0).bw <= kFusedStepMaxWidth) {
-    st = run_backward_slice(h, X, dY, nullptr, nullptr, 0, nb0, s, &o);
+  if (step_is_fused(L, batch)) {
+    st = run_backward_slice(h, X, dY, nullptr, nullptr, 0, (int)batch, s, &o);
   } else {
-    if (!L.d_gacc) {
-      size_t acct = 0;
-      cudaError_t e = snack::dev_alloc(&L.d_gacc, (size_t)L.nnz_pad, &acct);
-      if (e != cudaSuccess) return cuda_fail(h, e, "gradient buffer allocation");
-      account(L);
-    }
     for (int64_t b0 = 0; b0 < batch; b0 += snack::kMaxSlice) {
       const int nb = (int)std::min<int64_t>(snack::kMaxSlice, batch - b0);
       if ((st = run_backward_slice(h, X, dY, nullptr, L.d_gacc, b0, nb, s)) != SNACK_OK) return st;
@@ -360,6 +381,17 @@ bool finite(float x) { return x == x && x - x == 0.f; }
 }  // namespace
 
 namespace snack {
+cudaError_t device_malloc(void **p, size_t bytes) {
+  int64_t left = g_fail_alloc.load(std::memory_order_relaxed);
+  while (left >= 0 && !g_fail_alloc.compare_exchange_weak(left, left - 1)) {
+  }
+  if (left == 0) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMalloc(p, bytes);
+}
+
 // Failures of entry points that have no handle report through
 // snack_last_error(NULL), like snack_create.
 void record_thread_error(const std::string &msg) { g_create_error = msg; }
@@ -392,9 +424,9 @@ snack_status snack_create(int64_t out_features, int64_t in_features, int64_t nnz
   const float *uval = val;
   if (!ptrs_on_device && nnz > 0) {
     // Stage host arrays on the device.
-    if ((e = cudaMalloc(&d_row, nnz * 4)) != cudaSuccess ||
-        (e = cudaMalloc(&d_col, nnz * 4)) != cudaSuccess ||
-        (val && (e = cudaMalloc(&d_val, nnz * 4)) != cudaSuccess) ||
+    if ((e = snack::dev_alloc(&d_row, (size_t)nnz, nullptr)) != cudaSuccess ||
+        (e = snack::dev_alloc(&d_col, (size_t)nnz, nullptr)) != cudaSuccess ||
+        (val && (e = snack::dev_alloc(&d_val, (size_t)nnz, nullptr)) != cudaSuccess) ||
         (e = cudaMemcpyAsync(d_row, row, nnz * 4, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
         (e = cudaMemcpyAsync(d_col, col, nnz * 4, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
         (val && (e = cudaMemcpyAsync(d_val, val, nnz * 4, cudaMemcpyHostToDevice, s)) != cudaSuccess)) {
@@ -434,8 +466,8 @@ snack_status snack_create_random(int64_t out_features, int64_t in_features, int6
   h->L.in = in_features;
   std::string err;
   int32_t *d_row = nullptr, *d_col = nullptr;
-  if ((e = cudaMalloc(&d_row, std::max<int64_t>(nnz, 1) * 4)) != cudaSuccess ||
-      (e = cudaMalloc(&d_col, std::max<int64_t>(nnz, 1) * 4)) != cudaSuccess) {
+  if ((e = snack::dev_alloc(&d_row, (size_t)std::max<int64_t>(nnz, 1), nullptr)) != cudaSuccess ||
+      (e = snack::dev_alloc(&d_col, (size_t)std::max<int64_t>(nnz, 1), nullptr)) != cudaSuccess) {
     cudaFree(d_row);
     delete h;
     return fail(nullptr, SNACK_ERR_ALLOC, std::string("cudaMalloc: ") + cudaGetErrorString(e));
@@ -543,7 +575,8 @@ snack_status snack_sgd_step(snack_handle h, const float *X, const float *dY, int
   o.lr = lr;
   o.mom = momentum;
   o.wd = weight_decay;
-  if (momentum != 0.f && (st = ensure_opt_state(h, snack::kOptSgd, 1, s)) != SNACK_OK) return st;
+  if ((st = ensure_step_buffers(h, snack::kOptSgd, momentum != 0.f ? 1 : 0, batch, s)) != SNACK_OK)
+    return st;
   return run_opt_step(h, X, dY, batch, o, s);
 }
 
@@ -562,7 +595,7 @@ snack_status snack_adam_step(snack_handle h, const float *X, const float *dY, in
       (st = check_device(h)) != SNACK_OK)
     return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((st = ensure_opt_state(h, snack::kOptAdam, 2, s)) != SNACK_OK) return st;
+  if ((st = ensure_step_buffers(h, snack::kOptAdam, 2, batch, s)) != SNACK_OK) return st;
   const double bc1 = 1.0 - std::pow((double)beta1, (double)step);
   const double bc2 = 1.0 - std::pow((double)beta2, (double)step);
   snack::OptArgs o;
@@ -660,11 +693,15 @@ snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_wi
 
 uint64_t snack_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+void snack_debug_fail_alloc(int64_t after) {
+  g_fail_alloc.store(after < 0 ? -1 : after, std::memory_order_relaxed);
+}
+
 snack_status snack_selftest_wait(void *stream, int *timed_out) {
   if (!timed_out) return fail(nullptr, SNACK_ERR_INVALID_ARG, "timed_out is NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int *d = nullptr;
-  cudaError_t e = cudaMalloc(&d, sizeof(int));
+  cudaError_t e = snack::dev_alloc(&d, 1, nullptr);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "self-test flag allocation");
   int v = 0;
   if ((e = cudaMemsetAsync(d, 0, sizeof(int), s)) != cudaSuccess ||

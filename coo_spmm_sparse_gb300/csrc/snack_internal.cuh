@@ -169,10 +169,12 @@ cudaError_t launch_transpose_pair(const float *a, int64_t a_ld, int64_t a_cols, 
 cudaError_t launch_transpose(const float *src, int64_t ld, int nb, int64_t ncols, float *dst,
                              int bw, cudaStream_t s, bool pdl = false);
 
-// Topology (topology.cu).
+// Topology (topology.cu).  workspace = false leaves out the per-slice
+// workspace (transposed operands, error flag): a layer built only to take
+// another's topology.
 snack_status build_topology(Layer &L, int64_t nnz, const int32_t *d_row_user,
                             const int32_t *d_col_user, const float *d_val_user,
-                            cudaStream_t s, std::string &err);
+                            cudaStream_t s, std::string &err, bool workspace = true);
 snack_status draw_random_cells(int64_t out, int64_t in, int64_t count, uint64_t seed,
                                int32_t *d_row, int32_t *d_col, int64_t *trials,
                                cudaStream_t s, std::string &err);
@@ -183,12 +185,16 @@ void free_layer(Layer &L);
 // values pointer is out.
 snack_status refresh_csc_values(Layer &L, cudaStream_t s, std::string &err);
 
-// Device memory helper: cudaMalloc with byte accounting.
+// Every device allocation of the library: cudaMalloc, unless the
+// out-of-memory test hook (snack_debug_fail_alloc) makes this one fail.
+cudaError_t device_malloc(void **p, size_t bytes);
+
+// Device memory helper: device_malloc with byte accounting.
 template <typename T>
 cudaError_t dev_alloc(T **p, size_t count, size_t *acct) {
   size_t bytes = count * sizeof(T);
   if (bytes == 0) bytes = sizeof(T);
-  cudaError_t e = cudaMalloc(reinterpret_cast<void **>(p), bytes);
+  cudaError_t e = device_malloc(reinterpret_cast<void **>(p), bytes);
   if (e == cudaSuccess && acct) *acct += bytes;
   return e;
 }

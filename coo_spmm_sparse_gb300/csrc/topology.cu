@@ -10,6 +10,7 @@
 // These run once per topology change, never per training step; they may
 // allocate temporaries and synchronise the stream.
 #include <algorithm>
+#include <utility>
 #include <climits>
 #include <cmath>
 #include <cstring>
@@ -38,7 +39,7 @@ struct Temps {
   template <typename T>
   cudaError_t get(T **p, size_t count) {
     size_t bytes = std::max<size_t>(count * sizeof(T), 16);
-    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(p), bytes);
+    cudaError_t e = device_malloc(reinterpret_cast<void **>(p), bytes);
     if (e == cudaSuccess) ptrs.push_back(*p);
     return e;
   }
@@ -639,7 +640,7 @@ __global__ void carry_state(const uint32_t *src, int64_t n, const float *old, fl
 
 snack_status build_topology(Layer &L, int64_t nnz, const int32_t *d_row_user,
                             const int32_t *d_col_user, const float *d_val_user, cudaStream_t s,
-                            std::string &err) {
+                            std::string &err, bool workspace) {
   L.nnz = nnz;
   L.nnz_pad = pad4(nnz);
   size_t *acct = &L.device_bytes;
@@ -651,10 +652,12 @@ snack_status build_topology(Layer &L, int64_t nnz, const int32_t *d_row_user,
   TRY_CUDA(dev_alloc(&L.d_val_csc, L.nnz_pad, acct));
   TRY_CUDA(dev_alloc(&L.d_row_ptr, L.out + 1, acct));
   TRY_CUDA(dev_alloc(&L.d_col_ptr, L.in + 1, acct));
-  TRY_CUDA(dev_alloc(&L.d_xt, (size_t)L.in * kMaxSlice, acct));
-  TRY_CUDA(dev_alloc(&L.d_dyt, (size_t)L.out * kMaxSlice, acct));
-  TRY_CUDA(dev_alloc(&L.d_err, 1, acct));
-  TRY_CUDA(cudaMemsetAsync(L.d_err, 0, sizeof(int), s));
+  if (workspace) {
+    TRY_CUDA(dev_alloc(&L.d_xt, (size_t)L.in * kMaxSlice, acct));
+    TRY_CUDA(dev_alloc(&L.d_dyt, (size_t)L.out * kMaxSlice, acct));
+    TRY_CUDA(dev_alloc(&L.d_err, 1, acct));
+    TRY_CUDA(cudaMemsetAsync(L.d_err, 0, sizeof(int), s));
+  }
   TRY_CUDA(cudaMemsetAsync(L.d_col, 0, L.nnz_pad * 4, s));
   TRY_CUDA(cudaMemsetAsync(L.d_row, 0, L.nnz_pad * 4, s));
   TRY_CUDA(cudaMemsetAsync(L.d_val, 0, L.nnz_pad * 4, s));
@@ -719,6 +722,12 @@ snack_status draw_random_cells(int64_t out, int64_t in, int64_t count, uint64_t 
   return SNACK_OK;
 }
 
+// Magnitude prune + uniform regrow.  The new entry set (survivors and
+// regrown cells, its values and optimizer state) is built beside the layer,
+// as a second layer of the same shape; only once all of it exists is it
+// committed: values and state are copied into the layer's own buffers
+// (their pointers stay valid) and the topology arrays are swapped.  A
+// failure before that, an allocation included, leaves the layer as it was.
 snack_status prune_regrow(Layer &L, float frac, uint64_t seed, int64_t *pruned, int64_t *trials,
                           cudaStream_t s, std::string &err) {
   const int64_t n = L.nnz;
@@ -731,14 +740,19 @@ snack_status prune_regrow(Layer &L, float frac, uint64_t seed, int64_t *pruned, 
   uint64_t *ka, *kb, *fresh;
   uint32_t *va, *vb;
   unsigned char *gone;
-  float *old_val;
+  int32_t *new_row, *new_col;
+  float *new_val, *new_state[2] = {nullptr, nullptr};
   TRY_CUDA(t.get(&ka, n));
   TRY_CUDA(t.get(&kb, n));
   TRY_CUDA(t.get(&va, n));
   TRY_CUDA(t.get(&vb, n));
   TRY_CUDA(t.get(&fresh, P));
   TRY_CUDA(t.get(&gone, n));
-  TRY_CUDA(t.get(&old_val, n));
+  TRY_CUDA(t.get(&new_row, n));
+  TRY_CUDA(t.get(&new_col, n));
+  TRY_CUDA(t.get(&new_val, n));
+  for (int i = 0; i < 2; ++i)
+    if (L.d_opt[i]) TRY_CUDA(t.get(&new_state[i], n));
   TRY_CUDA(cudaMemsetAsync(gone, 0, n, s));
   magnitude_keys<<<grid_for(n, 256), 256, 0, s>>>(L.d_val, n, ka, va);
   TRY_CUDA(cudaGetLastError());
@@ -753,22 +767,53 @@ snack_status prune_regrow(Layer &L, float frac, uint64_t seed, int64_t *pruned, 
   // va still holds the magnitude order (a permutation of 0..n-1).
   merged_keys<<<grid_for(n, 256), 256, 0, s>>>(L.d_row, L.d_col, n, L.in, va, P, fresh, kb, vb);
   TRY_CUDA(cudaGetLastError());
-  TRY_CUDA(cudaMemcpyAsync(old_val, L.d_val, n * sizeof(float), cudaMemcpyDeviceToDevice, s));
   uint64_t *k1 = kb, *k2 = ka;
   uint32_t *v1 = vb, *v2 = va;
   st = radix_sort(&k1, &v1, &k2, &v2, n, bits_for(cells - 1), s, err);
   if (st != SNACK_OK) return st;
-  regrown_values<<<grid_for(n, 256), 256, 0, s>>>(k1, v1, n, L.in, old_val, L.d_row, L.d_col,
-                                                  L.d_val);
+  regrown_values<<<grid_for(n, 256), 256, 0, s>>>(k1, v1, n, L.in, L.d_val, new_row, new_col,
+                                                  new_val);
   TRY_CUDA(cudaGetLastError());
-  for (float *state : L.d_opt) {
-    if (!state) continue;
-    TRY_CUDA(cudaMemcpyAsync(old_val, state, n * sizeof(float), cudaMemcpyDeviceToDevice, s));
-    carry_state<<<grid_for(n, 256), 256, 0, s>>>(v1, n, old_val, state);
+  for (int i = 0; i < 2; ++i) {
+    if (!L.d_opt[i]) continue;
+    carry_state<<<grid_for(n, 256), 256, 0, s>>>(v1, n, L.d_opt[i], new_state[i]);
     TRY_CUDA(cudaGetLastError());
   }
-  TRY_CUDA(cudaStreamSynchronize(s));
-  return finish_layout(L, k1, s, err);
+  // The new layout beside the layer (canonical input: its sort keeps the order).
+  Layer N;
+  N.out = L.out;
+  N.in = L.in;
+  N.device = L.device;
+  st = build_topology(N, n, new_row, new_col, new_val, s, err, false);
+  if (st != SNACK_OK) {
+    free_layer(N);
+    return st;
+  }
+  // Commit: nothing below allocates.
+  cudaError_t e = cudaMemcpyAsync(L.d_val, N.d_val, n * sizeof(float), cudaMemcpyDeviceToDevice, s);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i)
+    if (L.d_opt[i])
+      e = cudaMemcpyAsync(L.d_opt[i], new_state[i], n * sizeof(float), cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    free_layer(N);
+    err = std::string("prune/regrow commit: ") + cudaGetErrorString(e);
+    return SNACK_ERR_CUDA;
+  }
+  std::swap(L.d_row, N.d_row);
+  std::swap(L.d_col, N.d_col);
+  std::swap(L.d_row_ptr, N.d_row_ptr);
+  std::swap(L.d_col_ptr, N.d_col_ptr);
+  std::swap(L.d_csc_row, N.d_csc_row);
+  std::swap(L.d_csc_perm, N.d_csc_perm);
+  std::swap(L.d_val_csc, N.d_val_csc);
+  std::swap(L.csr, N.csr);
+  std::swap(L.csc, N.csc);
+  std::swap(L.d_partial, N.d_partial);
+  std::swap(L.d_counter, N.d_counter);
+  L.csc_vals = !L.values_shared;  // the copy was derived from these values
+  free_layer(N);  // the old topology and the shadow's own values
+  return SNACK_OK;
 }
 
 snack_status refresh_csc_values(Layer &L, cudaStream_t s, std::string &err) {

@@ -314,6 +314,17 @@ snack_status snack_selftest_wait(void *stream, int *timed_out);
  */
 uint64_t snack_launch_count(void);
 
+/*
+ * Test hook for the out-of-memory paths: after `after` more device
+ * allocations by this library (0 = the next one), one allocation reports
+ * cudaErrorMemoryAllocation without allocating, and the hook disarms
+ * itself; a negative value disarms it.  Process-wide (all handles and
+ * threads).  A call that meets the failure returns SNACK_ERR_ALLOC, frees
+ * what it had allocated and leaves an existing handle as it was.  The paper
+ * has no counterpart; it exists so that those paths can be tested.
+ */
+void snack_debug_fail_alloc(int64_t after);
+
 int64_t snack_nnz(snack_handle h);
 int64_t snack_out_features(snack_handle h);
 int64_t snack_in_features(snack_handle h);
