@@ -364,18 +364,23 @@ def snack_destroy(h: SnackHandle):
 
 
 class _SnackFunction(torch.autograd.Function):
-    """Forward Y = X W^T; backward dX = dY W and dW at the stored entries."""
+    """Forward Y = X W^T; backward dX = dY W and dW at the stored entries.
+
+    The values tensor is saved with X, so autograd refuses a backward after
+    the values were changed in place between forward and backward."""
 
     @staticmethod
     def forward(ctx, X, values, handle):
         ctx.handle = handle
-        ctx.save_for_backward(X)
+        ctx.save_for_backward(X, values)
         return snack_forward(handle, X.contiguous())
 
     @staticmethod
     def backward(ctx, dY):
-        (X,) = ctx.saved_tensors
+        X, _ = ctx.saved_tensors
         need_dx, need_dw = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        if not (need_dx or need_dw):
+            return None, None, None
         dX, dW = snack_backward(ctx.handle, X.contiguous(), dY.contiguous(), need_dx=need_dx,
                                 need_dw=need_dw)
         return dX, dW, None
@@ -384,9 +389,17 @@ class _SnackFunction(torch.autograd.Function):
 class SnackLinear(torch.nn.Module):
     """Drop-in for nn.Linear whose weight exists only as its stored entries.
 
-    The weight values are a Parameter viewing the library's value array, so
-    optimizers update them in place.  Bias (optional) is a dense Parameter
-    added by PyTorch; it is not part of the sparse product."""
+    ``weight_values`` is a Parameter viewing the library's value array
+    (canonical order: rows ascending, columns ascending within a row), so a
+    torch optimizer updates the layer in place and its gradient arrives in
+    the same order.  Bias (optional) is a dense Parameter added by PyTorch;
+    it is not part of the sparse product.
+
+    The library keeps a column-ordered copy of the values for dX.  A write
+    to ``weight_values`` (an optimizer step) bumps the tensor's version
+    counter; the next forward sees the new version and has the library
+    re-derive the copy (one gather of the values) before it is used, so dX
+    never reads stale values and never takes the slower permutation path."""
 
     def __init__(self, in_features: int, out_features: int, nnz: int, seed: int,
                  std: float = 0.02, bias: bool = True):
@@ -398,8 +411,22 @@ class SnackLinear(torch.nn.Module):
         vals.copy_((torch.randn(nnz, generator=g) * std).to(vals.device))
         self.weight_values = torch.nn.Parameter(vals)
         self.bias = torch.nn.Parameter(torch.zeros(out_features, device=vals.device)) if bias else None
+        self._synced_version = None  # version of weight_values the copy was derived from
+
+    @property
+    def nnz(self) -> int:
+        return self.handle.nnz
+
+    def sync_values(self) -> None:
+        """Re-derive the library's column-ordered value copy if the values
+        changed since it was last derived (called by forward)."""
+        v = self.weight_values._version
+        if v != self._synced_version:
+            snack_values_changed(self.handle)
+            self._synced_version = v
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
+        self.sync_values()
         shape = x.shape
         y = _SnackFunction.apply(x.reshape(-1, self.in_features), self.weight_values, self.handle)
         y = y.reshape(*shape[:-1], self.out_features)
@@ -407,5 +434,18 @@ class SnackLinear(torch.nn.Module):
 
     @torch.no_grad()
     def prune_regrow(self, frac: float, seed: int):
-        """Topology step in place; the values Parameter keeps its storage."""
-        return snack_prune_regrow(self.handle, frac, seed)
+        """Topology step in place (magnitude prune + Algorithm 2 regrow,
+        canonical order restored).  ``weight_values`` keeps its storage and
+        now holds the survivors' values and zeros for the regrown entries,
+        in the new canonical order.  Optimizer state that torch keeps per
+        element of ``weight_values`` (momentum, Adam moments) is NOT
+        reordered: reset it after this call, or train with the library's
+        own steps (snack_sgd_step / snack_adam_step), whose state follows the
+        entries.  Returns (pruned, trials)."""
+        res = snack_prune_regrow(self.handle, frac, seed)
+        self._synced_version = self.weight_values._version  # the library re-derived the copy
+        return res
+
+    def export(self):
+        """(row, col, val) numpy arrays of the stored entries in canonical order."""
+        return snack_export(self.handle)

@@ -9,8 +9,9 @@
 // 10000 x 4 floats), each CTA (1024 threads) copies it once into shared
 // memory with cp.async.bulk (completion on an mbarrier, bounded wait), then
 // runs the usual segment loop gathering from there.
+#include <map>
 #include <mutex>
-#include <unordered_map>
+#include <utility>
 
 #include "spmm_dispatch.cuh"
 
@@ -105,21 +106,25 @@ __global__ void __launch_bounds__(kResidentThreads) sddmm_resident(const SddmmAr
 template <typename K, typename A>
 cudaError_t launch_resident(K kern, const A &a, int64_t n_op, int *err, size_t smem, bool pdl,
                             cudaStream_t s) {
+  // The shared-memory limit is a per-device attribute of the kernel: the
+  // record of limits already raised is keyed by (device, kernel).
   static std::mutex mu;
-  static std::unordered_map<const void *, size_t> raised;
-  const void *key = reinterpret_cast<const void *>(kern);
+  static std::map<std::pair<int, const void *>, size_t> raised;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const std::pair<int, const void *> key(dev, reinterpret_cast<const void *>(kern));
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = raised.find(key);
     if (it == raised.end() || it->second < smem) {
-      cudaError_t e =
-          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       raised[key] = smem;
     }
   }
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kResidentThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kResidentThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int64_t need = (a.nseg * a.lps + kResidentThreads - 1) / kResidentThreads;

@@ -4,24 +4,27 @@
 // parallel.
 #pragma once
 
+#include <map>
 #include <mutex>
-#include <unordered_map>
 #include <utility>
 
 #include "spmm_kernels.cuh"
 
 namespace snack {
 
-// Resident blocks per SM of a kernel (queried once per kernel).
+// Resident blocks per SM of a kernel (queried once per device and kernel).
 inline int resident_blocks(const void *kern) {
   static std::mutex mu;
-  static std::unordered_map<const void *, int> cache;
+  static std::map<std::pair<int, const void *>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  const std::pair<int, const void *> key(dev, kern);
   std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(kern);
+  auto it = cache.find(key);
   if (it != cache.end()) return it->second;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 256, 0) != cudaSuccess || n < 1) n = 1;
-  cache.emplace(kern, n);
+  cache.emplace(key, n);
   return n;
 }
 

@@ -167,6 +167,14 @@ extern "C" snack_status snack_forward_csr_static(int64_t out_features, int64_t i
       (nnz > 0 && (!aligned(col, 16) || !aligned(val, 16))))
     return fail(SNACK_ERR_INVALID_ARG,
                 "col, val, X and Y must be 16-byte aligned, row_ptr 4-byte aligned");
+  {
+    // At batch 1 the kernel reads X itself while other teams write Y, so an
+    // in-place call would silently give wrong rows: refuse overlapping ranges.
+    const uintptr_t x0 = reinterpret_cast<uintptr_t>(X), y0 = reinterpret_cast<uintptr_t>(Y);
+    const uintptr_t x1 = x0 + (uintptr_t)batch * (uintptr_t)in_features * 4u;
+    const uintptr_t y1 = y0 + (uintptr_t)batch * (uintptr_t)out_features * 4u;
+    if (x0 < y1 && y0 < x1) return fail(SNACK_ERR_INVALID_ARG, "Y overlaps X");
+  }
   const int first_width = slice_width(batch < kStaticSlice ? batch : kStaticSlice);
   if (first_width > 1 && in_features * first_width > kStaticScratchFloats)
     return fail(SNACK_ERR_UNSUPPORTED,
@@ -181,6 +189,8 @@ extern "C" snack_status snack_forward_csr_static(int64_t out_features, int64_t i
   {
     // First call on a device: look up the device address of the scratch
     // array (host code cannot use the symbol itself as a device pointer).
+    // The address is kept for the life of the process; a cudaDeviceReset()
+    // unloads the module and makes it stale (the header says so).
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (!g_scratch_addr[dev]) {
       void *addr = nullptr;

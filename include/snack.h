@@ -256,12 +256,13 @@ snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_wi
 /*
  * Forward pass Y = X W^T for callers that cannot allocate device memory.
  * The paper has no counterpart to this entry point; it exists for callers
- * that hold no allocation rights when they run the layer: code that runs
- * while a CUDA graph is captured in global mode (cudaMalloc is not allowed
- * there), serving loops whose device memory is already reserved by another
- * allocator, and latency-critical paths where an allocation's implicit
- * device synchronisation is not acceptable.  It needs no handle and
- * allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * that hold no allocation rights when they run the layer: serving loops
+ * whose device memory is already reserved by another allocator (a pool that
+ * has taken all free memory at start-up), latency-critical paths where an
+ * allocation's implicit device synchronisation is not acceptable, and
+ * plug-in code running inside a host framework that owns all device
+ * allocation.  It needs no handle and allocates nothing: no cudaMalloc,
+ * cudaFree or allocating library call.
  *
  *   row_ptr [out_features+1], col [nnz], val [nnz]: a CSR layout of W in the
  *     caller's device memory, e.g. as exported by snack_export_segments()
@@ -277,10 +278,14 @@ snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_wi
  * scratch for batch 1) must not exceed 2^21, else SNACK_ERR_UNSUPPORTED.
  * The scratch is rewritten in full by every call.  All calls share it:
  * calls whose work overlaps on the GPU (other streams, other threads) race.
- * The first call on a device looks up the scratch's device address; make
- * that first call before any stream capture.  Rows are not split, so a few
- * very long rows run slower than with snack_forward().  Errors are reported
- * through snack_last_error(NULL).  Asynchronous on `stream`.
+ * The first call on a device looks up the scratch's device address and
+ * keeps it for the life of the process; make that first call before any
+ * stream capture.  cudaDeviceReset() unloads the library's device code and
+ * makes the kept address stale: do not call this entry point on a device
+ * after resetting it.  Y must not overlap X (SNACK_ERR_INVALID_ARG).  Rows
+ * are not split, so a few very long rows run slower than with
+ * snack_forward().  Errors are reported through snack_last_error(NULL).
+ * Asynchronous on `stream`.
  */
 snack_status snack_forward_csr_static(int64_t out_features, int64_t in_features, int64_t nnz,
                                       const int32_t *row_ptr, const int32_t *col,
