@@ -5,32 +5,37 @@ One step = forward (Y = X W^T), backward-input (dX = dY W) and
 backward-weight (dW at the stored entries) of every layer of the workload at
 every batch size of the workload, through the library's C ABI.  The metric
 is effective GFLOP/s, 2 * nnz * batch per SpMM, three SpMMs per (layer,
-batch).  Default workload: the GPT-2-small MLP projections 3072x768 and
-768x3072 at 95% sparsity, batch 1, 8 and 32.
+batch).  Default workload: the 10000x10000 single-layer sweep (the paper's
+§4.2 training cycle layer) at 90, 95 and 99 % sparsity (10 M, 5 M and 1 M
+stored entries), batch 1, 4, 8, 16 and 64.
 
 Timing: W warm-up steps, then K steps, each replayed from a CUDA graph of
 the step and timed with CUDA events on the launching stream; between steps
 a 256 MiB buffer (about twice the L2) is written and then read back, so
 every step starts with a cold L2 holding only clean lines (the flush's own
 write-backs are not charged to the step).  Barrier + synchronize on both
-sides; the max over ranks is reported.  Under torchrun every rank runs its own replica (weak scaling, no
-collective on the data path).
+sides; the max over ranks is reported.  Under torchrun every rank runs its
+own replica (weak scaling, no collective on the data path).
 
 Also reported: the roofline of the dominant op (metric bytes / measured
-duration against the measured HBM copy bandwidth), an end-to-end number
-through the same calls with host buffers (one pinned H2D copy of every X and
-dY, one D2H copy of every Y, dX and dW, inside the timed region), the CPU oracle on the host cores on a
-bounded sample, the SM clocks sampled during the timed region, and the
-kernel launches.  The per-op table (each op replayed from its own CUDA graph,
-10 untimed then 50 timed replays, each after an L2 flush; mean and median
-microseconds) gives GFLOP/s, GB/s of the metric's bytes, the fraction of
-the measured copy peak, and gather_gbs: the 4 * B bytes per stored entry of
-operand rows every op gathers (through L1 or shared memory), the bound that
-takes over from HBM as B grows.  It also times the Adam step
-(snack_adam_step) of each layer and batch; it is not part of the metric.
+duration against the measured HBM copy bandwidth) and of the ops at the
+95 % / batch >= 8 operating point, an end-to-end number through the same
+calls with host buffers (one pinned H2D copy of every X and dY, one D2H copy
+of every Y, dX and dW, inside the timed region), the CPU oracle on the host
+cores on a bounded sample (single-threaded, and its all-cores copy), the SM
+clocks sampled during the timed region, and the kernel launches.  The per-op
+table (each op replayed from its own CUDA graph, 10 untimed then 50 timed
+replays, each after an L2 flush; mean and median microseconds) gives
+GFLOP/s, GB/s of the metric's bytes, the fraction of the measured copy peak,
+and gather_gbs: the 4 * B bytes per stored entry of operand rows every op
+gathers (through L1 or shared memory), the bound that takes over from HBM as
+B grows.  It also times the Adam step (snack_adam_step) of each layer and
+batch, a training step (forward, backward-input, Adam step) on the 95 %
+layer, and the forward / backward ops of the GPT-2 MLP layers and the skewed
+8192x8192 layer; none of these are part of the metric.
 
 `--impl reference` times the CPU oracle instead (the deliberately slow
-reference arm), on the same workload and metric.
+reference arm), on a bounded sample of the same workload and metric.
 """
 
 from __future__ import annotations
@@ -231,6 +236,121 @@ def recorded_traffic(kernel: str, workload: str):
 
 # ------------------------------------------------------------------ our arm
 
+def _upload(cases, dev, stream, sn):
+    import torch
+    with torch.cuda.stream(stream):
+        for c in cases:
+            L = c["layer"]
+            c["h"] = sn.snack_create(L.out, L.inp, c["row"], c["col"], c["val"], stream=stream)
+            c["dev"] = {}
+            for B, (X, dY) in c["acts"].items():
+                c["dev"][B] = dict(X=torch.from_numpy(X).to(dev), dY=torch.from_numpy(dY).to(dev),
+                                   Y=torch.empty(B, L.out, device=dev),
+                                   dX=torch.empty(B, L.inp, device=dev),
+                                   dW=torch.empty(L.nnz, device=dev))
+    torch.cuda.synchronize()
+
+
+def time_graph(fn, stream, flush, reps=50, warm=10):
+    """Mean and median microseconds of `fn` replayed from a CUDA graph between
+    events on `stream`, after an L2 flush each time."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        for _ in range(warm):
+            g.replay()
+        ts = []
+        for _ in range(reps):
+            flush_l2(flush)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            ts.append((e0, e1))
+    torch.cuda.synchronize()
+    del g
+    durs = [a.elapsed_time(b) * 1e3 for a, b in ts]
+    return statistics.mean(durs), statistics.median(durs)
+
+
+def op_rows(cases, sn, stream, flush, ops=("fwd", "bwd_input", "bwd_weight", "adam_step"),
+            workload=None):
+    """Per-op table of one workload's layers and batches."""
+    import torch
+    rows = []
+
+    def run_op(op, c, d):
+        if op == "fwd":
+            sn.snack_forward(c["h"], d["X"], d["Y"], stream=stream)
+        elif op == "bwd_input":
+            sn.snack_backward_input(c["h"], d["dY"], d["dX"], stream=stream)
+        elif op == "bwd_weight":
+            sn.snack_backward_weight(c["h"], d["X"], d["dY"], d["dW"], stream=stream)
+        else:  # Adam step (gradient + update); not part of the metric
+            sn.snack_adam_step(c["h"], d["X"], d["dY"], lr=1e-3, step=1, stream=stream)
+
+    for c in cases:
+        L = c["layer"]
+        for B, d in c["dev"].items():
+            for op in ops:
+                if op == "adam_step":  # its first call allocates the moments
+                    with torch.cuda.stream(stream):
+                        run_op(op, c, d)
+                    torch.cuda.synchronize()
+                us, med = time_graph(lambda: run_op(op, c, d), stream, flush)
+                if op == "adam_step":  # the steps changed the values: re-derive
+                    sn.snack_values_changed(c["h"])  # their column-ordered copy
+                    torch.cuda.synchronize()
+                nbytes = metric_bytes(op, L.nnz, L.out, L.inp, B)
+                plan_op = {"fwd": 0, "bwd_input": 1}.get(op, 2)  # dW and Adam: rows
+                bw, lanes, segs = sn.snack_plan(c["h"], plan_op, B)
+                r = dict(op=op, layer=L.name, shape=f"{L.out}x{L.inp}", nnz=L.nnz, B=B,
+                         us=round(us, 3), us_median=round(med, 3),
+                         gflops=round(2 * L.nnz * B / us / 1e3, 2),
+                         gbs=round(nbytes / us / 1e3, 1), bytes=nbytes,
+                         gather_gbs=round(4 * B * L.nnz / us / 1e3, 1),
+                         plan=dict(slice=bw, lanes=lanes, segments=segs))
+                if workload:
+                    r["workload"] = workload
+                rows.append(r)
+    return rows
+
+
+def train_step_rows(case, sn, stream, flush, batches=(1, 16)):
+    """One training step of a layer (forward, backward-input, Adam step), two
+    ways: dX reading the values through the column permutation (the
+    column-ordered copy left stale by the step) and dX reading the copy,
+    re-derived right after the step.  Not part of the metric."""
+    import torch
+    rows = []
+    c = case
+    L = c["layer"]
+    h = c["h"]
+    for B in batches:
+        d = c["dev"][B]
+        for mode in ("permutation", "refreshed_copy"):
+            def fn():
+                sn.snack_forward(h, d["X"], d["Y"], stream=stream)
+                sn.snack_backward_input(h, d["dY"], d["dX"], stream=stream)
+                sn.snack_adam_step(h, d["X"], d["dY"], lr=1e-3, step=1, stream=stream)
+                if mode == "refreshed_copy":
+                    sn.snack_values_changed(h, stream=stream)
+            with torch.cuda.stream(stream):
+                sn.snack_adam_step(h, d["X"], d["dY"], lr=1e-3, step=1, stream=stream)
+                if mode == "refreshed_copy":
+                    sn.snack_values_changed(h, stream=stream)
+            torch.cuda.synchronize()
+            us, med = time_graph(fn, stream, flush)
+            rows.append(dict(op="train_step", mode=mode, layer=L.name, shape=f"{L.out}x{L.inp}",
+                             nnz=L.nnz, B=B, us=round(us, 3), us_median=round(med, 3),
+                             gflops=round(3 * 2 * L.nnz * B / us / 1e3, 2)))
+    sn.snack_values_changed(h)
+    torch.cuda.synchronize()
+    return rows
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -244,19 +364,7 @@ def run_ours(args):
     wl, cases = make_cases(args.workload, args.batches, args.seed)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    with torch.cuda.stream(stream):
-        for c in cases:
-            L = c["layer"]
-            c["h"] = sn.snack_create(L.out, L.inp, c["row"], c["col"], c["val"], stream=stream)
-            c["dev"] = {}
-            for B, (X, dY) in c["acts"].items():
-                Xd = torch.from_numpy(X).to(dev)
-                dYd = torch.from_numpy(dY).to(dev)
-                c["dev"][B] = dict(X=Xd, dY=dYd,
-                                   Y=torch.empty(B, L.out, device=dev),
-                                   dX=torch.empty(B, L.inp, device=dev),
-                                   dW=torch.empty(L.nnz, device=dev))
-    torch.cuda.synchronize()
+    _upload(cases, dev, stream, sn)
 
     def step():
         for c in cases:
@@ -302,70 +410,40 @@ def run_ours(args):
     total_ms = reduce_max(sum(step_ms), dev)
     fl = flops_per_step(cases)
     value = world * fl * args.steps / (total_ms / 1e3) / 1e9
+    del graph
 
     # Per-op durations -> dominant op, roofline.  Each op is replayed from its
     # own CUDA graph between events on the launching stream, after an L2
     # flush that keeps the GPU busy while the host queues the replay.
-    ops = []
-    reps = 50  # per op: 50 timed replays after 10 untimed ones
-
-    def run_op(op, c, d):
-        if op == "fwd":
-            sn.snack_forward(c["h"], d["X"], d["Y"], stream=stream)
-        elif op == "bwd_input":
-            sn.snack_backward_input(c["h"], d["dY"], d["dX"], stream=stream)
-        elif op == "bwd_weight":
-            sn.snack_backward_weight(c["h"], d["X"], d["dY"], d["dW"], stream=stream)
-        else:  # Adam step (gradient + update); not part of the metric
-            sn.snack_adam_step(c["h"], d["X"], d["dY"], lr=1e-3, step=1, stream=stream)
-
-    with torch.cuda.stream(stream):
-        for c in cases:
-            L = c["layer"]
-            for B, d in c["dev"].items():
-                for op in ("fwd", "bwd_input", "bwd_weight", "adam_step"):
-                    if op == "adam_step":  # its first call allocates the moments
-                        run_op(op, c, d)
-                        torch.cuda.synchronize()
-                    g_op = torch.cuda.CUDAGraph()
-                    with torch.cuda.graph(g_op, stream=stream):
-                        run_op(op, c, d)
-                    for _ in range(10):
-                        g_op.replay()
-                    ts = []
-                    for _ in range(reps):
-                        flush_l2(flush)
-                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                        e0.record(stream)
-                        g_op.replay()
-                        e1.record(stream)
-                        ts.append((e0, e1))
-                    torch.cuda.synchronize()
-                    del g_op
-                    if op == "adam_step":  # the steps changed the values: re-derive
-                        sn.snack_values_changed(c["h"])  # their column-ordered copy
-                        torch.cuda.synchronize()
-                    durs = [a.elapsed_time(b) * 1e3 for a, b in ts]
-                    us = statistics.mean(durs)
-                    nbytes = metric_bytes(op, L.nnz, L.out, L.inp, B)
-                    plan_op = {"fwd": 0, "bwd_input": 1}.get(op, 2)  # dW and Adam: rows
-                    bw, lanes, segs = sn.snack_plan(c["h"], plan_op, B)
-                    ops.append(dict(op=op, layer=L.name, shape=f"{L.out}x{L.inp}", nnz=L.nnz, B=B,
-                                    us=round(us, 3), us_median=round(statistics.median(durs), 3),
-                                    gflops=round(2 * L.nnz * B / us / 1e3, 2),
-                                    gbs=round(nbytes / us / 1e3, 1), bytes=nbytes,
-                                    gather_gbs=round(4 * B * L.nnz / us / 1e3, 1),
-                                    plan=dict(slice=bw, lanes=lanes, segments=segs)))
+    ops = op_rows(cases, sn, stream, flush)
+    train = []
+    c95 = next((c for c in cases if c["layer"].name == "large95"), None)
+    if c95 is not None and not args.no_extra_ops:
+        train = train_step_rows(c95, sn, stream, flush,
+                                [B for B in (1, 16) if B in c95["dev"]])
+    extra = []
+    if not args.no_extra_ops:
+        for name in [w for w in args.extra_ops.split(",") if w and w != args.workload]:
+            _, xc = make_cases(name, None, args.seed)
+            _upload(xc, dev, stream, sn)
+            extra += op_rows(xc, sn, stream, flush, ops=("fwd", "bwd_input", "bwd_weight"),
+                             workload=name)
+            for c in xc:
+                c["h"].close()
+            del xc
     peak, peak_kind = read_peak()
-    for o in ops:
+    for o in ops + extra:
         o["frac"] = round(o["gbs"] / peak, 4)
     dom = max((o for o in ops if o["op"] != "adam_step"), key=lambda o: o["us"])
     tr = recorded_traffic(f"{dom['op']}:{dom['layer']}:B{dom['B']}", args.workload)
+    target = {f"{o['op']} B={o['B']}": o["frac"] for o in ops
+              if o["layer"] == "large95" and o["B"] >= 8 and o["op"] != "adam_step"}
     roofline = {"bound": "hbm", "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": dom["frac"], "traffic": tr,
                 "kernel": f"{dom['op']} {dom['shape']} nnz={dom['nnz']} B={dom['B']}",
                 "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
-                "bytes": "metric bytes nnz*12 + dense operands, per launch"}
+                "bytes": "metric bytes nnz*12 + dense operands, per launch",
+                "at_95pct_batch_ge_8": target}
 
     # End to end through the same calls with host buffers: each step's inputs
     # (X, dY of every layer and batch) travel in one pinned buffer with one
@@ -461,6 +539,8 @@ def run_ours(args):
             "clocks": clk,
             "wall_s_timed_region": round(wall, 4),
             "ops": ops,
+            "train_step": train,
+            "extra_ops": extra,
         }
         print(json.dumps(line), flush=True)
 
@@ -476,39 +556,104 @@ def describe(wl, cases):
 
 # ------------------------------------------------------------------ oracle
 
-def oracle_step(prepared):
-    import oracle
-    for p in prepared:
-        L, ref = p["layer"], p["ref"]
-        for B, (X, dY) in p["acts"].items():
-            oracle.forward(L.out, L.inp, ref["row"], ref["col"], ref["val"], X)
-            oracle.backward_input(L.out, L.inp, ref["row"], ref["col"], ref["val"], dY)
-            oracle.backward_weight(L.out, L.inp, ref["row"], ref["col"], X, dY)
+SAMPLE_ENTRIES = 600_000  # stored entries per layer the oracle sample keeps at most
 
 
-def prepare_oracle(cases):
+def prepare_oracle(cases, max_entries: int = SAMPLE_ENTRIES):
+    """A bounded sample of every layer for the oracle: a stride of its rows
+    (forward and dW: the sampled rows' entries, a layer of those rows) and
+    the same stride of its columns (backward-input: the sampled columns'
+    entries), each canonicalised once.  The stride keeps at most
+    max_entries entries per layer; the flops are counted on the sample."""
+    import numpy as np
     import oracle
     oracle.build()
-    return [dict(layer=c["layer"], acts=c["acts"],
-                 ref=oracle.canonicalize(c["layer"].out, c["layer"].inp, c["row"], c["col"],
-                                         c["val"])) for c in cases]
+    prepared = []
+    for c in cases:
+        L = c["layer"]
+        ref = oracle.canonicalize(L.out, L.inp, c["row"], c["col"], c["val"])
+        stride = max(1, -(-L.nnz // max_entries))
+        rows = np.arange(0, L.out, stride)
+        cols = np.arange(0, L.inp, stride)
+        rmap = np.full(L.out, -1, np.int64)
+        rmap[rows] = np.arange(rows.size)
+        cmap = np.full(L.inp, -1, np.int64)
+        cmap[cols] = np.arange(cols.size)
+        rk = rmap[ref["row"]] >= 0
+        ck = cmap[ref["col"]] >= 0
+        rsub = oracle.canonicalize(rows.size, L.inp, rmap[ref["row"][rk]], ref["col"][rk],
+                                   ref["val"][rk])
+        csub = oracle.canonicalize(L.out, cols.size, ref["row"][ck], cmap[ref["col"][ck]],
+                                   ref["val"][ck])
+        acts = {B: (X, dY, np.ascontiguousarray(dY[:, rows]))
+                for B, (X, dY) in c["acts"].items()}
+        prepared.append(dict(out=L.out, inp=L.inp, nr=rows.size, nc=cols.size, rsub=rsub,
+                             csub=csub, acts=acts, stride=stride))
+    return prepared
 
 
-def cpu_baseline(cases, budget_s: float = 10.0):
-    """The oracle as it stands (single-threaded C, fp64 accumulation), timed on
-    whole steps of the same workload until about budget_s of CPU work."""
-    prepared = prepare_oracle(cases)
-    fl = flops_per_step(cases)
+def oracle_sample_flops(prepared) -> float:
+    return float(sum(2 * B * (2 * p["rsub"]["row"].size + p["csub"]["row"].size)
+                     for p in prepared for B in p["acts"]))
+
+
+def oracle_step(prepared, omp_threads: int = 0):
+    """One pass of the oracle over the sample: forward and dW on the sampled
+    rows, backward-input on the sampled columns, every batch.  omp_threads > 0
+    runs the all-cores copy of the same loops (bit-identical results)."""
+    import oracle
+    for p in prepared:
+        r, cs = p["rsub"], p["csub"]
+        for B, (X, dY, dYr) in p["acts"].items():
+            if omp_threads:
+                oracle.forward_omp(p["nr"], p["inp"], r, X, omp_threads)
+                oracle.backward_input_omp(p["out"], p["nc"], cs, dY, omp_threads)
+                oracle.backward_weight_omp(p["nr"], p["inp"], r, X, dYr, omp_threads)
+            else:
+                oracle.forward(p["nr"], p["inp"], r["row"], r["col"], r["val"], X)
+                oracle.backward_input(p["out"], p["nc"], cs["row"], cs["col"], cs["val"], dY)
+                oracle.backward_weight(p["nr"], p["inp"], r["row"], r["col"], X, dYr)
+
+
+def _sample_text(prepared):
+    ents = sum(p["rsub"]["row"].size + p["csub"]["row"].size for p in prepared)
+    strides = sorted({p["stride"] for p in prepared})
+    return (f"every {'/'.join(map(str, strides))}-th row (fwd, dW) and column (dX) of each "
+            f"layer, all batches: {ents} sampled entries")
+
+
+def _timed_passes(prepared, budget_s, omp_threads=0):
     t0 = time.perf_counter()
     n = 0
     while True:
-        oracle_step(prepared)
+        oracle_step(prepared, omp_threads)
         n += 1
         el = time.perf_counter() - t0
         if el >= budget_s or el / n * (n + 1) > 3 * budget_s:
-            break
-    return {"value": round(fl * n / el / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} whole step(s) of the workload, {el:.1f} s, single thread"}
+            return n, el
+
+
+def cpu_baseline(cases, budget_s: float = 10.0):
+    """The oracle as it stands (single-threaded C, fp64 accumulation) on a
+    bounded sample of the workload, ~budget_s of CPU work; then its all-cores
+    copy (same loops split over the host's cores, bit-identical results) on
+    the same sample."""
+    import oracle
+    prepared = prepare_oracle(cases)
+    fl = oracle_sample_flops(prepared)
+    n, el = _timed_passes(prepared, budget_s)
+    res = {"value": round(fl * n / el / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": f"{_sample_text(prepared)}; {n} pass(es), {el:.1f} s, single thread"}
+    try:
+        cores = oracle.host_cores()
+        oracle_step(prepared, cores)  # warm the threads
+        n2, el2 = _timed_passes(prepared, budget_s / 2, cores)
+        res["all_cores"] = {"value": round(fl * n2 / el2 / 1e9, 4), "unit": UNIT,
+                            "cores": cores, "kind": "oracle loops on all cores (OpenMP)",
+                            "sample": f"same sample; {n2} pass(es), {el2:.1f} s"}
+    except Exception as e:  # no OpenMP build on this host
+        res["all_cores"] = {"unavailable": str(e)[:200]}
+    return res
 
 
 def run_reference(args):
@@ -517,7 +662,7 @@ def run_reference(args):
         return
     wl, cases = make_cases(args.workload, args.batches, args.seed)
     prepared = prepare_oracle(cases)
-    fl = flops_per_step(cases)
+    fl = oracle_sample_flops(prepared)
     for _ in range(args.warmup):
         oracle_step(prepared)
     t0 = time.perf_counter()
@@ -532,7 +677,7 @@ def run_reference(args):
             "data": "synthetic", "impl": "reference",
             "config": {"workload": describe(wl, cases)},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"{args.steps} whole step(s) of the workload"},
+                             "sample": f"{_sample_text(prepared)}; one pass per step"},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -611,12 +756,17 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gpt2_mlp",
-                    help="gpt2_mlp (default), toy256, large90/95/99, skewed, gpt2_decoder")
+    ap.add_argument("--workload", default="large",
+                    help="large (default: 10000x10000 at 90/95/99 %%), large90/95/99, gpt2_mlp, "
+                         "toy256, skewed, gpt2_decoder")
     ap.add_argument("--batches", type=lambda s: [int(x) for x in s.split(",")], default=None)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra-ops", default="gpt2_mlp,skewed",
+                    help="workloads whose ops are timed too (per-op table only)")
+    ap.add_argument("--no-extra-ops", action="store_true",
+                    help="skip the extra workloads and the training-step timing")
     ap.add_argument("--only-op", choices=["fwd", "bwd_input", "bwd_weight", "bwd"], default=None,
                     help="profiling mode: run one op --reps times on one layer (--layer) and "
                          "the first batch of the workload (cold L2 before each), print no JSON")

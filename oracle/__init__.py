@@ -16,6 +16,12 @@ CPU-baseline leg of ``bench.py`` do.  The arithmetic lives in
 * ``uniform_init``        §3.3 Algorithm 2 (getrand = counter SplitMix64)
 * ``prune_regrow``        Appendix G (magnitude prune, Algorithm 2 regrow)
 
+``snack_oracle_omp.c`` holds an all-cores copy of the three product loops
+(``forward_omp``, ``backward_input_omp``, ``backward_weight_omp``) for the
+benchmark's CPU baseline: the same terms summed in the same order per output
+element, split over threads by whole rows / columns / entries, so its
+results are bit-identical to the single-threaded routines.
+
 Every function is pinned by ``tests/test_oracle_pins.py`` against something
 other than itself (Table 7, dense matmul, scipy.sparse, closed forms,
 published generator outputs, brute force on tiny inputs).
@@ -64,6 +70,104 @@ def build(force: bool = False) -> str:
     with open(stamp, "w") as f:
         f.write(platform.machine())
     return _LIB_PATH
+
+
+_OMP_SRC = os.path.join(_HERE, "snack_oracle_omp.c")
+_OMP_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle_omp.so")
+_omp_lib = None
+
+
+def build_omp(force: bool = False) -> str:
+    """Compile snack_oracle_omp.c (gcc -fopenmp) into oracle/_build/."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stamp = os.path.join(_BUILD_DIR, "machine_omp.txt")
+    try:
+        with open(stamp) as f:
+            same_machine = f.read().strip() == platform.machine()
+    except OSError:
+        same_machine = False
+    if (not force and same_machine and os.path.exists(_OMP_LIB_PATH)
+            and os.path.getmtime(_OMP_LIB_PATH) >= os.path.getmtime(_OMP_SRC)):
+        return _OMP_LIB_PATH
+    tmp = _OMP_LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+                           "-fno-fast-math", "-ffp-contract=off",
+                           _OMP_SRC, "-o", tmp, "-lm"])
+    os.replace(tmp, _OMP_LIB_PATH)
+    with open(stamp, "w") as f:
+        f.write(platform.machine())
+    return _OMP_LIB_PATH
+
+
+def _load_omp():
+    global _omp_lib
+    with _lock:
+        if _omp_lib is not None:
+            return _omp_lib
+        lib = ctypes.CDLL(build_omp())
+        i64, p, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        lib.oracle_omp_threads.restype = ci
+        lib.oracle_omp_forward.argtypes = [i64, i64, p, p, p, i64, p, p, p, ci]
+        lib.oracle_omp_backward_input.argtypes = [i64, i64, p, p, p, p, i64, p, p, p, ci]
+        lib.oracle_omp_backward_weight.argtypes = [i64, i64, i64, p, p, i64, p, p, p, p, ci]
+        for fn in (lib.oracle_omp_forward, lib.oracle_omp_backward_input,
+                   lib.oracle_omp_backward_weight):
+            fn.restype = ci
+        _omp_lib = lib
+        return lib
+
+
+def host_cores() -> int:
+    """CPU cores this process may run on (its affinity mask)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def forward_omp(out: int, inp: int, ref: dict, X, threads: int | None = None):
+    """Y = X W^T on all cores; ``ref`` is a canonicalize() result.  Returns (Y, S),
+    bit-identical to forward() on ref's canonical arrays."""
+    lib = _load_omp()
+    X = _c(X, np.float32)
+    B = X.shape[0]
+    assert X.shape == (B, inp)
+    Y = np.empty((B, out), np.float32)
+    S = np.empty((B, out), np.float64)
+    lib.oracle_omp_forward(out, inp, _ptr(_c(ref["row_ptr"], np.int32)),
+                           _ptr(_c(ref["col"], np.int32)), _ptr(_c(ref["val"], np.float32)), B,
+                           _ptr(X), _ptr(Y), _ptr(S), threads or host_cores())
+    return Y, S
+
+
+def backward_input_omp(out: int, inp: int, ref: dict, dY, threads: int | None = None):
+    """dX = dY W on all cores (column-partitioned).  Returns (dX, S)."""
+    lib = _load_omp()
+    dY = _c(dY, np.float32)
+    B = dY.shape[0]
+    assert dY.shape == (B, out)
+    dX = np.empty((B, inp), np.float32)
+    S = np.empty((B, inp), np.float64)
+    lib.oracle_omp_backward_input(out, inp, _ptr(_c(ref["col_ptr"], np.int32)),
+                                  _ptr(_c(ref["csc_perm"], np.int32)),
+                                  _ptr(_c(ref["row"], np.int32)), _ptr(_c(ref["val"], np.float32)),
+                                  B, _ptr(dY), _ptr(dX), _ptr(S), threads or host_cores())
+    return dX, S
+
+
+def backward_weight_omp(out: int, inp: int, ref: dict, X, dY, threads: int | None = None):
+    """dW at the stored entries on all cores.  Returns (dW, S)."""
+    lib = _load_omp()
+    X, dY = _c(X, np.float32), _c(dY, np.float32)
+    B = X.shape[0]
+    assert X.shape == (B, inp) and dY.shape == (B, out)
+    n = ref["row"].size
+    dW = np.empty(n, np.float32)
+    S = np.empty(n, np.float64)
+    lib.oracle_omp_backward_weight(out, inp, n, _ptr(_c(ref["row"], np.int32)),
+                                   _ptr(_c(ref["col"], np.int32)), B, _ptr(X), _ptr(dY),
+                                   _ptr(dW), _ptr(S), threads or host_cores())
+    return dW, S
 
 
 def _load():

@@ -49,7 +49,8 @@ def test_reference_arm_line():
 
 @pytest.mark.gpu
 def test_our_arm_line():
-    d = _bench("--workload", "toy256", "--steps", "3", "--warmup", "3", "--cpu-seconds", "1")
+    d = _bench("--workload", "toy256", "--steps", "3", "--warmup", "3", "--cpu-seconds", "1",
+               "--no-extra-ops")
     _common(d, 3, 3)
     assert d.get("impl", "ours") != "reference"
     r = d["roofline"]
@@ -59,6 +60,7 @@ def test_our_arm_line():
     assert r["traffic"] is None or r["traffic"] > 0
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
+    assert cb["all_cores"]["cores"] >= 1 and cb["all_cores"]["value"] > 0
     assert d["gpu_launches"] > 0
     c = d["clocks"]
     assert c["sm_mhz"] > 0 and c["sm_max_mhz"] > 0 and isinstance(c["reasons"], list)

@@ -512,3 +512,32 @@ def test_adam_first_step_closed_form():
     got, m, v = oracle.adam_update(val, g, z, z, 0.01, 0.9, 0.999, 1e-8, 0.0, 1)
     assert np.allclose(got, val - 0.01 * g / (np.abs(g) + 1e-8), rtol=1e-15, atol=0)
     assert np.allclose(m, 0.1 * g) and np.allclose(v, 0.001 * g * g)
+
+
+# ------------------------------------------------------------ all-cores copy
+
+@pytest.mark.parametrize("shape,sp,B", [((300, 200), 90, 5), ((64, 3000), 99, 1),
+                                        ((2000, 1500), 97, 17)])
+def test_omp_copy_is_bit_identical_to_the_oracle(shape, sp, B):
+    # The CPU baseline's all-cores copy of the three product loops must give
+    # the single-threaded oracle's bits (same terms, same order per output),
+    # whatever the thread count.
+    import workloads
+    out, inp = shape
+    nnz = workloads.nnz_for(out, inp, sp)
+    row, col = workloads.uniform_pattern(out, inp, nnz, sp)
+    val = workloads.normal(nnz, 0.1, sp, 0)
+    ref = oracle.canonicalize(out, inp, row, col, val)
+    g = np.random.default_rng(sp + B)
+    X = g.standard_normal((B, inp)).astype(np.float32)
+    dY = g.standard_normal((B, out)).astype(np.float32)
+    want = (oracle.forward(out, inp, ref["row"], ref["col"], ref["val"], X),
+            oracle.backward_input(out, inp, ref["row"], ref["col"], ref["val"], dY),
+            oracle.backward_weight(out, inp, ref["row"], ref["col"], X, dY))
+    for threads in (1, 3, oracle.host_cores()):
+        got = (oracle.forward_omp(out, inp, ref, X, threads),
+               oracle.backward_input_omp(out, inp, ref, dY, threads),
+               oracle.backward_weight_omp(out, inp, ref, X, dY, threads))
+        for (a, sa), (b, sb) in zip(got, want):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+            assert np.array_equal(sa, sb)

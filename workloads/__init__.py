@@ -173,6 +173,7 @@ def workload(name: str, seed: int = 0) -> Workload:
     toy256     256x256 at 90%, values N(0, 1/sqrt(nnz/out)), batch 4
     gpt2_mlp   768->3072 and 3072->768 at 95%, values N(0, 0.02), batch 1/8/32
     large{90,95,99}  10000x10000, values N(0, 1/sqrt(in)), batch 1/4/16/64
+    large      the three 10000x10000 layers together, batch 1/4/8/16/64
     skewed     8192x8192 at 99%, rank-Zipf(1.1) rows, values N(0, 1), batch 1/16
     gpt2_decoder  12 blocks x (c_attn 768->2304, attn c_proj 768->768,
                c_fc 768->3072, mlp c_proj 3072->768) at 99%, 256 tokens
@@ -185,6 +186,11 @@ def workload(name: str, seed: int = 0) -> Workload:
         return Workload(name, [Layer("c_fc", 3072, 768, 95, val_std=0.02, seed=seed),
                                Layer("c_proj", 768, 3072, 95, val_std=0.02, seed=seed + 1)],
                         [1, 8, 32])
+    if name == "large":
+        # the whole 10000x10000 sweep: 90 / 95 / 99 %, batches 1-64 (8 added
+        # for the batch >= 8 operating point)
+        return Workload(name, [Layer(f"large{sp}", 10000, 10000, sp, val_std=0.01, seed=seed)
+                               for sp in (90, 95, 99)], [1, 4, 8, 16, 64])
     if name.startswith("large"):
         sp = int(name[5:] or 95)
         return Workload(name, [Layer(f"large{sp}", 10000, 10000, sp, val_std=0.01,
