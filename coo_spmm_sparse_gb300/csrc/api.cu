@@ -71,6 +71,7 @@ void account(snack::Layer &L) {
   b += (size_t)L.nnz_pad * 4 * 5;  // col, row, val, csc_row, csc_perm
   b += (size_t)(L.out + 1 + L.in + 1) * 4;
   b += (size_t)(L.csr.nseg + L.csr.nsplit + L.csc.nseg + L.csc.nsplit) * sizeof(int4);
+  b += (size_t)(L.csr.panel.ctas + L.csc.panel.ctas) * 32 * sizeof(int4);
   b += (size_t)(L.in + L.out) * snack::kMaxSlice * 4;
   b += (size_t)std::max(L.csr.nslots, L.csc.nslots) * snack::kMaxSlice * 4;
   b += (size_t)std::max(L.csr.nsplit, L.csc.nsplit) * 4;
@@ -164,6 +165,22 @@ cudaError_t launch_cols(const snack::Layer &L, const snack::Plan &p, snack::Spmm
   return a.perm ? snack::launch_spmm_cols(q, a, true, s) : snack::launch_spmm_rows(q, a, true, s);
 }
 
+// Column-panel launch arguments of one direction (rows: the forward and
+// dW, operand X^T; columns: dX, operand dY^T).
+snack::PanelArgs panel_args(snack::Layer &L, bool rows, const float *op, int nb) {
+  snack::PanelArgs a = {};
+  a.ptr = rows ? L.d_row_ptr : L.d_col_ptr;
+  a.idx = rows ? L.d_col : L.d_csc_row;
+  a.val = rows || !L.csc_vals ? L.d_val : L.d_val_csc;
+  a.perm = rows ? nullptr : L.d_csc_perm;
+  a.src = op;
+  a.n_op = rows ? L.in : L.out;
+  a.ld = rows ? L.out : L.in;
+  a.nb = nb;
+  a.err = L.d_err;
+  return a;
+}
+
 // Forward Y = X W^T over batch slices of at most 256: the slice of X is
 // transposed into the workspace (not needed for a single row), then the
 // row-segment kernel runs.  Every launch is a programmatic dependent of the
@@ -183,10 +200,18 @@ snack_status run_forward(snack_handle h, const float *X, float *Y, int64_t batch
       g_launches.fetch_add(1, std::memory_order_relaxed);
       op = L.d_xt;
     }
+    cudaError_t e;
+    if (snack::panel_fits(L.csr.panel, p.bw)) {
+      snack::PanelArgs pa = panel_args(L, true, op, nb);
+      pa.dst = Y + b0 * L.out;
+      e = snack::launch_panel(snack::kPanelSpmm, p.bw, L.csr.panel, pa, true, s);
+      if (e != cudaSuccess) return cuda_fail(h, e, "forward launch");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+      continue;
+    }
     snack::SpmmArgs a = spmm_args(L, true, op, Y + b0 * L.out, nb);
     a.prefetch = transposed;
     a.stride = p.bw;
-    cudaError_t e;
     if (snack::resident_fits(p.bw, L.in, L.csr.nseg, L.nnz)) {
       e = snack::launch_resident_spmm(false, p, a, L.in, L.d_err, true, s);
     } else {
@@ -247,6 +272,39 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     if (opt) rows.opt = *opt;
   }
   cudaError_t e;
+  const bool pan_c = dX && snack::panel_fits(L.csc.panel, pc.bw);
+  const bool pan_r = want_w && !fused_opt && snack::panel_fits(L.csr.panel, pr.bw);
+  if (pan_c || pan_r) {
+    // Column-panel kernels for at least one product: one launch per product,
+    // the second a programmatic dependent of the first.
+    if (dX) {
+      if (pan_c) {
+        snack::PanelArgs pa = panel_args(L, false, dyt, nb);
+        pa.dst = dX + b0 * L.in;
+        e = snack::launch_panel(L.csc_vals ? snack::kPanelSpmm : snack::kPanelSpmmPerm, pc.bw,
+                                L.csc.panel, pa, true, s);
+      } else {
+        e = launch_cols(L, pc, cols, nb, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(h, e, "backward-input launch");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    if (want_w) {
+      if (pan_r) {
+        snack::PanelArgs pa = panel_args(L, true, xt, nb);
+        pa.dyt = dyt;
+        pa.dw = dW;
+        pa.accumulate = b0 > 0;
+        e = snack::launch_panel(snack::kPanelSddmm, pr.bw, L.csr.panel, pa, true, s);
+      } else {
+        rows.nsub = sddmm_subranges(L.csr, pr);
+        e = snack::launch_sddmm(pr, rows, true, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(h, e, "backward-weight launch");
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    return SNACK_OK;
+  }
   const bool res_c = dX && snack::resident_fits(pc.bw, L.out, L.csc.nseg, L.nnz);
   const bool res_r = want_w && !fused_opt && snack::resident_fits(pr.bw, L.in, L.csr.nseg, L.nnz);
   if (want_w && !res_r) rows.nsub = sddmm_subranges(L.csr, pr);
@@ -687,7 +745,11 @@ snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_wi
   if (lanes_per_segment) *lanes_per_segment = p.lanes;
   if (segments) *segments = t.nseg;
   if (resident)
-    *resident = snack::resident_fits(p.bw, op == 1 ? h->L.out : h->L.in, t.nseg, h->L.nnz) ? 1 : 0;
+    *resident = snack::panel_fits(t.panel, p.bw)
+                    ? 2
+                    : (snack::resident_fits(p.bw, op == 1 ? h->L.out : h->L.in, t.nseg, h->L.nnz)
+                           ? 1
+                           : 0);
   return SNACK_OK;
 }
 

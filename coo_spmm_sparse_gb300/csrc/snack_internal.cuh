@@ -36,6 +36,19 @@ namespace snack {
 constexpr int kMaxSlice = 256;  // widest batch slice one kernel launch handles
 constexpr int kOptNone = 0, kOptSgd = 1, kOptAdam = 2;  // optimizer kinds
 
+// Entry-balanced partition of a line table for the column-panel kernels
+// (panel.cu): per CTA 32 int4, warps 0-30 {first entry, end entry, first
+// line, lines} and {first line, end line} of the CTA.  Built at topology
+// time for layers of at least panel_min_nnz() entries.
+constexpr int kPanelLinesPerWarp = 4;  // lines one consumer warp can hold
+constexpr int kPanelSpmm = 0, kPanelSpmmPerm = 1, kPanelSddmm = 2;  // panel kernel modes
+
+struct PanelTable {
+  int4 *d_part = nullptr;  // [ctas][32]
+  int64_t ctas = 0;
+  int lines_max = 0;       // most lines any consumer warp covers
+};
+
 struct SegTable {
   int64_t nseg = 0;
   int64_t nsplit = 0;
@@ -44,6 +57,7 @@ struct SegTable {
   int64_t max_len = 0;     // longest line
   int4 *d_seg = nullptr;   // [nseg]
   int4 *d_split = nullptr; // [nsplit]
+  PanelTable panel;        // column-panel partition (d_part null when not built)
 };
 
 struct Layer {
@@ -125,6 +139,24 @@ struct SddmmArgs {
   OptArgs opt;       // optimizer step fused in instead of writing dw (slices of 1-4)
 };
 
+// Everything a column-panel launch needs (panel.cu).
+struct PanelArgs {
+  const int4 *part;      // the table's partition (set by the launcher)
+  const int32_t *ptr;    // line pointer [lines + 1]
+  const int32_t *idx;    // operand index of each entry, line order
+  const float *val;      // values in line order (canonical, or the column-ordered copy)
+  const int32_t *perm;   // column order -> canonical position (kPanelSpmmPerm)
+  const float *src;      // transposed operand [n_op][bw]
+  int64_t n_op;          // operand lines
+  float *dst;            // SpMM output, element (b, line) at dst[b * ld + line]
+  int64_t ld;
+  int nb;                // valid batch rows of the slice
+  const float *dyt;      // dW: transposed dY [lines][bw]
+  float *dw;             // dW output (canonical order)
+  int accumulate;        // dW: add to dw (batch slices after the first)
+  int *err;              // the layer's device error flag
+};
+
 // Kernel selection: batch slice width, lanes per entry group, lanes per segment.
 struct Plan {
   int bw = 1;
@@ -156,6 +188,15 @@ cudaError_t launch_backward_fused(const Plan &pc, const SpmmArgs &cols, const Pl
 bool resident_fits(int bw, int64_t n_op, int64_t nseg, int64_t nnz);
 cudaError_t launch_resident_spmm(bool perm, const Plan &p, const SpmmArgs &a, int64_t n_op,
                                  int *err, bool pdl, cudaStream_t s);
+// Column-panel kernels (slices of 8-64 floats) on a table with a partition.
+bool panel_fits(const PanelTable &t, int bw);
+cudaError_t launch_panel(int mode, int bw, const PanelTable &t, const PanelArgs &a, bool pdl,
+                         cudaStream_t s);
+void build_panel_partition(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz, int ctas,
+                           std::vector<int4> &part, int *lines_max);
+// Smallest layer (stored entries) that gets panel partitions: 2^21, or the
+// SNACK_PANEL_MIN_NNZ environment variable when set.
+int64_t panel_min_nnz();
 // One block that waits, with a short bound, on an mbarrier nothing completes
 // and sets *err when it gives up (the failure path of the bounded waits).
 cudaError_t launch_wait_selftest(int *err, cudaStream_t s);

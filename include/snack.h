@@ -246,9 +246,11 @@ snack_status snack_export_segments(snack_handle h, int32_t *row_ptr, int32_t *co
  * batch slice width (1, 2, 4, 8, 16, 32, 64, 128 or 256), the lanes that
  * share one row (or column) segment (the launch may halve them when that
  * keeps every segment in one wave of resident teams), the number of
- * segments, and whether every block holds the whole dense operand in shared
- * memory (1) or gathers it from global memory (0).  Any output may be NULL.
- * Pure host query.
+ * segments, and where the dense operand is gathered from: 0 = global memory
+ * (through L1), 1 = a copy of the whole operand in every block's shared
+ * memory, 2 = shared memory one column panel at a time (the column-panel
+ * kernels of slices of 8-64 floats on layers with a panel partition).  Any
+ * output may be NULL.  Pure host query.
  */
 snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_width,
                         int32_t *lanes_per_segment, int64_t *segments, int32_t *resident);
