@@ -104,6 +104,14 @@ __host__ __device__ constexpr int panel_lines() {
   return kStageBytes / (4 * BW);
 }
 
+// Batch-slice shape of the panel kernels: G = BW / 4 lanes per entry, each
+// holding one 16-byte vector of the row (a 64-float row is read by 16 lanes
+// with one instruction: two rows per 512-byte access, no bank conflict).
+template <int BW>
+struct PanelShape {
+  static constexpr int VEC = 4, NV = 1, G = BW / 4;
+};
+
 // One quad (entries kb..kb+3) of the index / value streams.
 template <int MODE>
 __device__ __forceinline__ void panel_quad(const PanelArgs &a, int kb, int (&c)[4], float (&w)[4]) {
@@ -127,6 +135,44 @@ __device__ __forceinline__ void panel_quad(const PanelArgs &a, int kb, int (&c)[
   }
 }
 
+// dW of one quad: d[e] holds each lane's part of entry e's dot product
+// (its 4 floats of the batch).  A butterfly over the G lanes of the group
+// sums and spreads at once: the first level leaves each lane two of the four
+// entries, the second one, and the remaining levels finish the sum; with
+// G = 2 / 4 / 8 / 16 the group spends 2 / 3 / 4 / 5 shuffles on its four
+// entries, and lane sub ends with entry (sub / (G / 4)) when G >= 4 (of
+// those, the lanes with sub % (G / 4) == 0 store it), or, for G = 2, with
+// entries 2 sub and 2 sub + 1.
+template <int G>
+__device__ __forceinline__ void panel_dw_store(const PanelArgs &a, int kb, int sub,
+                                               const bool (&t)[4], float (&d)[4]) {
+  const unsigned m = 0xffffffffu;
+  const bool up = (sub & (G / 2)) != 0;  // level 1: keep entries 2-3 (up) or 0-1
+  const float s0 = __shfl_xor_sync(m, up ? d[0] : d[2], G / 2);
+  const float s1 = __shfl_xor_sync(m, up ? d[1] : d[3], G / 2);
+  d[0] = (up ? d[2] : d[0]) + s0;
+  d[1] = (up ? d[3] : d[1]) + s1;
+  const int base = up ? 2 : 0;
+  if constexpr (G == 2) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      if (t[base + e]) {
+        float *dst = a.dw + kb + base + e;
+        *dst = a.accumulate ? *dst + d[e] : d[e];
+      }
+  } else {
+    const bool up2 = (sub & (G / 4)) != 0;  // level 2: keep one entry
+    d[0] = (up2 ? d[1] : d[0]) + __shfl_xor_sync(m, up2 ? d[0] : d[1], G / 4);
+#pragma unroll
+    for (int off = G / 8; off >= 1; off >>= 1) d[0] += __shfl_xor_sync(m, d[0], off);
+    const int e = base + (up2 ? 1 : 0);
+    if ((sub & (G / 4 - 1)) == 0 && t[e]) {
+      float *dst = a.dw + kb + e;
+      *dst = a.accumulate ? *dst + d[0] : d[0];
+    }
+  }
+}
+
 // Forward / dX epilogue of a consumer warp: reduce the lines' sums over the
 // groups, then write them out.  A line that starts in this warp's range is
 // this warp's to write; its parts in later warps (a line cut by warp
@@ -134,11 +180,11 @@ __device__ __forceinline__ void panel_quad(const PanelArgs &a, int kb, int (&c)[
 // entries get zeros.
 template <int BW, int RW>
 __device__ __forceinline__ void panel_spmm_out(const PanelArgs &a,
-                                               float (&acc)[RW][SliceShape<BW>::NV]
-                                                           [SliceShape<BW>::VEC],
+                                               float (&acc)[RW][PanelShape<BW>::NV]
+                                                           [PanelShape<BW>::VEC],
                                                const int4 *part, float *slot, int warp, int lane,
                                                int nl, int first, int W0, int W1) {
-  using S = SliceShape<BW>;
+  using S = PanelShape<BW>;
   constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
   const int grp = lane / G, sub = lane % G;
 #pragma unroll
@@ -190,7 +236,7 @@ __device__ __forceinline__ void panel_spmm_out(const PanelArgs &a,
 
 template <int BW, int RW, int MODE>
 __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs a) {
-  using S = SliceShape<BW>;
+  using S = PanelShape<BW>;
   constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
   constexpr int PW = panel_lines<BW>();
   static_assert(PW * BW * 4 == kStageBytes, "panel size");
@@ -200,6 +246,7 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
   float *slot = smem_f + kStages * PW * BW;               // [kConsumers][BW]
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
   __shared__ int4 part[32];
+  __shared__ int lstate[kConsumers * 3 * RW];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid < 32) part[tid] = a.part[(int64_t)blockIdx.x * 32 + tid];
@@ -260,34 +307,38 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
   const int grp = lane / G, sub = lane % G;
   const int4 me = part[warp];
   const int W0 = me.x, W1 = me.y, first = me.z, nl = me.w;
-  // Per line: cursor (first entry not yet taken), end of the warp's part,
-  // and the operand index at the cursor once known (a line whose next entry
-  // lies in a later panel is skipped without touching its streams).
-  int kcur[RW], kend[RW], cnext[RW];
+  // Per line j of the warp, kept in shared memory (registers go to the
+  // sums and the stream look-ahead): cursor (first entry not yet taken), end
+  // of the warp's part, and the operand index at the cursor once known, so
+  // that a line whose next entry lies in a later panel is skipped without
+  // touching its streams.
+  int *cur = lstate + warp * 3 * RW, *end = cur + RW, *nxt = end + RW;
   float acc[RW][NV][VEC];  // forward / dX: line sums; dW: the line's dY slice
 #pragma unroll
   for (int j = 0; j < RW; ++j) {
-    kcur[j] = 0;
-    kend[j] = 0;
-    cnext[j] = 0;
-    if (j < nl) {
-      const int r = first + j;
-      kcur[j] = max(a.ptr[r], W0);
-      kend[j] = min(a.ptr[r + 1], W1);
-    }
 #pragma unroll
     for (int v = 0; v < NV; ++v)
 #pragma unroll
       for (int i = 0; i < VEC; ++i) acc[j][v][i] = 0.f;
-    if constexpr (MODE == kPanelSddmm) {
-      if (j < nl) {
-        const float *p = a.dyt + (int64_t)(first + j) * BW + sub * VEC;
+    if (j < nl) {
+      const int r = first + j;
+      if (lane == 0) {
+        cur[j] = max(a.ptr[r], W0);
+        end[j] = min(a.ptr[r + 1], W1);
+        nxt[j] = 0;
+      }
+      if constexpr (MODE == kPanelSddmm) {
+        const float *p = a.dyt + (int64_t)r * BW + sub * VEC;
 #pragma unroll
         for (int v = 0; v < NV; ++v) load_vec<VEC>(p + v * G * VEC, acc[j][v]);
       }
     }
   }
+  __syncwarp();
 
+  // Entries gathered together: all four of a quad, two at a time when each
+  // lane holds two vectors of the row (64-float slices).
+  constexpr int EB = NV == 1 ? 4 : 2;
   bool ok = true;
   for (int p = 0; p < npanels && ok; ++p) {
     const int s = p % kStages;
@@ -296,93 +347,106 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
       if (lane == 0) atomicOr(a.err, 1);
       break;
     }
-    const float *st = stage + (size_t)s * PW * BW + sub * VEC;
-    const int pend = (p + 1) * PW;  // entries of this panel have index < pend
+    const int pbase = p * PW;
+    const float *st = stage + (size_t)s * PW * BW + sub * VEC - (int64_t)pbase * BW;
+    const int pend = pbase + PW;  // entries of this panel have operand index < pend
 #pragma unroll
     for (int j = 0; j < RW; ++j) {
-      if (j >= nl || cnext[j] >= pend) continue;
-      int k = kcur[j];
-      const int k1 = kend[j];
-      while (k < k1) {  // warp-uniform
-        const int kb = (k & ~3) + 4 * grp;
-        int c[4] = {0, 0, 0, 0};
-        float w[4] = {0.f, 0.f, 0.f, 0.f};
-        if (kb < k1) panel_quad<MODE>(a, kb, c, w);
-        bool take[4];
-        int cnt = 0, first_beyond = 0x7fffffff;
+      if (j >= nl || nxt[j] >= pend) continue;
+      int k = cur[j];
+      const int k1 = end[j];
+      int kb = (k & ~3) + 4 * grp;  // this group's quad
+      int c[4] = {0, 0, 0, 0};
+      float w[4] = {0.f, 0.f, 0.f, 0.f};
+      if (kb < k1) panel_quad<MODE>(a, kb, c, w);
+      int cn_at = 0x7fffffff;
+      while (true) {  // warp-uniform
+        // the next step's quad is in flight while this one is used
+        const int kbn = kb + 4 * (32 / G);
+        int cn[4] = {0, 0, 0, 0};
+        float wn[4] = {0.f, 0.f, 0.f, 0.f};
+        if (kbn < k1) panel_quad<MODE>(a, kbn, cn, wn);
+        const int lo = k - kb, hi = k1 - kb;  // entry e is in range iff lo <= e < hi
+        bool t[4];
+        int cnt = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const bool in = kb + e >= k && kb + e < k1;
-          take[e] = in && c[e] < pend;
-          if (in && c[e] >= pend) first_beyond = min(first_beyond, c[e]);
-          cnt += take[e] ? 1 : 0;
+          t[e] = e >= lo && e < hi && c[e] < pend;
+          cnt += t[e] ? 1 : 0;
         }
-        float x[4][NV][VEC];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-#pragma unroll
-          for (int v = 0; v < NV; ++v) {
-            if (take[e]) {
-              load_op<VEC, true>(st + (c[e] & (PW - 1)) * BW + v * G * VEC, x[e][v]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < VEC; ++i) x[e][v][i] = 0.f;
-            }
-          }
         if constexpr (MODE == kPanelSddmm) {
-          float res[4];
+          float d[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float d = 0.f;
+          for (int e0 = 0; e0 < 4; e0 += EB) {
+            float x[EB][NV][VEC];
 #pragma unroll
-            for (int v = 0; v < NV; ++v)
+            for (int e = 0; e < EB; ++e)
+              if (t[e0 + e])
 #pragma unroll
-              for (int i = 0; i < VEC; ++i) d = fmaf(acc[j][v][i], x[e][v][i], d);
+                for (int v = 0; v < NV; ++v)
+                  load_op<VEC, true>(st + c[e0 + e] * BW + v * G * VEC, x[e][v]);
 #pragma unroll
-            for (int off = 1; off < G; off <<= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-            res[e] = d;
-          }
-          if (sub == 0) {
-            float *dwp = a.dw + kb;
-            if (take[0] && take[1] && take[2] && take[3]) {
-              float4 o = make_float4(res[0], res[1], res[2], res[3]);
-              if (a.accumulate) {
-                const float4 old = *reinterpret_cast<const float4 *>(dwp);
-                o.x += old.x;
-                o.y += old.y;
-                o.z += old.z;
-                o.w += old.w;
-              }
-              *reinterpret_cast<float4 *>(dwp) = o;
-            } else {
+            for (int e = 0; e < EB; ++e) {
+              float q = 0.f;
+              if (t[e0 + e])
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (take[e]) dwp[e] = a.accumulate ? dwp[e] + res[e] : res[e];
+                for (int v = 0; v < NV; ++v)
+#pragma unroll
+                  for (int i = 0; i < VEC; ++i) q = fmaf(acc[j][v][i], x[e][v][i], q);
+              d[e0 + e] = q;
             }
           }
+          panel_dw_store<G>(a, kb, sub, t, d);
         } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
+          for (int e0 = 0; e0 < 4; e0 += EB) {
+            float x[EB][NV][VEC];
 #pragma unroll
-            for (int v = 0; v < NV; ++v)
+            for (int e = 0; e < EB; ++e)
+              if (t[e0 + e])
 #pragma unroll
-              for (int i = 0; i < VEC; ++i)
-                acc[j][v][i] = fmaf(take[e] ? w[e] : 0.f, x[e][v][i], acc[j][v][i]);
+                for (int v = 0; v < NV; ++v)
+                  load_op<VEC, true>(st + c[e0 + e] * BW + v * G * VEC, x[e][v]);
+#pragma unroll
+            for (int e = 0; e < EB; ++e)
+              if (t[e0 + e])
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+#pragma unroll
+                  for (int i = 0; i < VEC; ++i)
+                    acc[j][v][i] = fmaf(w[e0 + e], x[e][v][i], acc[j][v][i]);
+          }
         }
-        // The taken entries are a prefix of [k, k1): advance past them; stop
-        // at the first entry of a later panel.
-        const int total = __reduce_add_sync(0xffffffffu, (unsigned)cnt) / G;
+        // The taken entries are a prefix of [k, k1) (a line's entries are
+        // sorted by operand index): advance past them; stop at the first
+        // entry of a later panel.
+        const int total = (int)(__reduce_add_sync(0xffffffffu, (unsigned)cnt) / G);
+        const int step_end = (k & ~3) + 4 * (32 / G);
+        const int in_step = min(k1, step_end) - k;
+        const int k_old = k;
         k += total;
-        // entries of a line are sorted: the smallest index past the panel is
-        // the one at the new cursor
-        const int nxt = (int)__reduce_min_sync(0xffffffffu, (unsigned)first_beyond);
-        if (nxt != 0x7fffffff) {
-          cnext[j] = nxt;
+        if (total < in_step) {
+          // operand index of the entry now at the cursor, from the group
+          // whose quad holds it
+          const int comp = k & 3;
+          const int mine = comp == 0 ? c[0] : comp == 1 ? c[1] : comp == 2 ? c[2] : c[3];
+          cn_at = __shfl_sync(0xffffffffu, mine, ((k - (k_old & ~3)) >> 2) * G);
           break;
         }
+        if (k >= k1) break;
+        kb = kbn;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          c[e] = cn[e];
+          w[e] = wn[e];
+        }
       }
-      kcur[j] = k;
-      if (k >= k1) cnext[j] = 0x7fffffff;  // the warp's part of this line is done
+      __syncwarp();
+      if (lane == 0) {
+        cur[j] = k;
+        nxt[j] = cn_at;  // INT_MAX once the warp's part of the line is done
+      }
+      __syncwarp();
     }
     __syncwarp();
     if (lane == 0) bar_arrive(&empty[s]);
