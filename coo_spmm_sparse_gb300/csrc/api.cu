@@ -71,7 +71,7 @@ void account(snack::Layer &L) {
   b += (size_t)L.nnz_pad * 4 * 5;  // col, row, val, csc_row, csc_perm
   b += (size_t)(L.out + 1 + L.in + 1) * 4;
   b += (size_t)(L.csr.nseg + L.csr.nsplit + L.csc.nseg + L.csc.nsplit) * sizeof(int4);
-  b += (size_t)(L.csr.panel.ctas + L.csc.panel.ctas) * 32 * sizeof(int4);
+  b += L.csr.panel.bytes + L.csc.panel.bytes;
   b += (size_t)(L.in + L.out) * snack::kMaxSlice * 4;
   b += (size_t)std::max(L.csr.nslots, L.csc.nslots) * snack::kMaxSlice * 4;
   b += (size_t)std::max(L.csr.nsplit, L.csc.nsplit) * 4;

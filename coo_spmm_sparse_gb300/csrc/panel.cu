@@ -17,10 +17,14 @@
 //    stream (the CTA's lines are a row-aligned, entry-balanced share of the
 //    table; its 31 warps split that share evenly), covering at most RW
 //    lines.  Entries of a line are sorted by the operand index, so the part
-//    of a line that falls in panel p is the next run of its entries: the
-//    warp keeps a cursor per line and, for each resident panel, walks each
-//    line's run in steps of one quad (4 entries) per group of G lanes,
-//    gathering the operand rows from shared memory.
+//    of a line that falls in panel p is one run of consecutive entries; a
+//    table built with the topology holds every line's run offsets for every
+//    panel.  For each resident panel the warp walks its lines' runs in steps
+//    of one quad (4 entries) per group of G lanes, gathering the operand rows
+//    from shared memory.  Every step's address is known in advance (the next
+//    quad of the run, or the first of the next non-empty run, in this panel
+//    or the next), so the next step's index / value loads are always in
+//    flight while the current step gathers.
 //  * forward / dX: the lines' sums stay in registers across all panels.  At
 //    the end each warp reduces them over its groups; lines wholly inside a
 //    warp's range are written directly, a line cut by warp boundaries is
@@ -246,7 +250,6 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
   float *slot = smem_f + kStages * PW * BW;               // [kConsumers][BW]
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
   __shared__ int4 part[32];
-  __shared__ int lstate[kConsumers * 3 * RW];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid < 32) part[tid] = a.part[(int64_t)blockIdx.x * 32 + tid];
@@ -305,14 +308,18 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
 
   // ------------------------------------------------------------ consumers
   const int grp = lane / G, sub = lane % G;
+  constexpr int STEP = 4 * (32 / G);  // entries per warp step
   const int4 me = part[warp];
   const int W0 = me.x, W1 = me.y, first = me.z, nl = me.w;
-  // Per line j of the warp, kept in shared memory (registers go to the
-  // sums and the stream look-ahead): cursor (first entry not yet taken), end
-  // of the warp's part, and the operand index at the cursor once known, so
-  // that a line whose next entry lies in a later panel is skipped without
-  // touching its streams.
-  int *cur = lstate + warp * 3 * RW, *end = cur + RW, *nxt = end + RW;
+  // Run offsets of line j (lane j < RW holds them): lo = its first entry
+  // in panel p, hi = first entry in panel p + 1, hh = in panel p + 2.
+  const bool holder = lane < nl;
+  const int32_t *offl = a.off + first + lane;
+  int lo = 0, hi = 0, hh = 0;
+  if (holder) {
+    lo = offl[0];
+    hi = npanels >= 1 ? offl[(int64_t)a.lines] : lo;
+  }
   float acc[RW][NV][VEC];  // forward / dX: line sums; dW: the line's dY slice
 #pragma unroll
   for (int j = 0; j < RW; ++j) {
@@ -320,60 +327,75 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
     for (int v = 0; v < NV; ++v)
 #pragma unroll
       for (int i = 0; i < VEC; ++i) acc[j][v][i] = 0.f;
-    if (j < nl) {
-      const int r = first + j;
-      if (lane == 0) {
-        cur[j] = max(a.ptr[r], W0);
-        end[j] = min(a.ptr[r + 1], W1);
-        nxt[j] = 0;
-      }
-      if constexpr (MODE == kPanelSddmm) {
-        const float *p = a.dyt + (int64_t)r * BW + sub * VEC;
+    if constexpr (MODE == kPanelSddmm) {
+      if (j < nl) {
+        const float *p = a.dyt + (int64_t)(first + j) * BW + sub * VEC;
 #pragma unroll
         for (int v = 0; v < NV; ++v) load_vec<VEC>(p + v * G * VEC, acc[j][v]);
       }
     }
   }
-  __syncwarp();
 
-  // Entries gathered together: all four of a quad, two at a time when each
-  // lane holds two vectors of the row (64-float slices).
-  constexpr int EB = NV == 1 ? 4 : 2;
+  // The quad of the step at pre (a step base, multiple of 4), loaded ahead.
+  int pre = -1;
+  int c[4] = {0, 0, 0, 0};
+  float w[4] = {0.f, 0.f, 0.f, 0.f};
+  constexpr int EB = 2;  // entries gathered together
   bool ok = true;
   for (int p = 0; p < npanels && ok; ++p) {
     const int s = p % kStages;
+    // the offsets closing panel p + 1: used by the look-ahead at the end of
+    // this panel, loaded now
+    if (holder && p + 2 <= npanels) hh = offl[(int64_t)(p + 2) * a.lines];
     ok = bar_wait(&full[s], (uint32_t)((p / kStages) & 1));
     if (!ok) {
       if (lane == 0) atomicOr(a.err, 1);
       break;
     }
-    const int pbase = p * PW;
-    const float *st = stage + (size_t)s * PW * BW + sub * VEC - (int64_t)pbase * BW;
-    const int pend = pbase + PW;  // entries of this panel have operand index < pend
+    const float *st = stage + (size_t)s * PW * BW + sub * VEC - (int64_t)p * PW * BW;
 #pragma unroll
     for (int j = 0; j < RW; ++j) {
-      if (j >= nl || nxt[j] >= pend) continue;
-      int k = cur[j];
-      const int k1 = end[j];
-      int kb = (k & ~3) + 4 * grp;  // this group's quad
-      int c[4] = {0, 0, 0, 0};
-      float w[4] = {0.f, 0.f, 0.f, 0.f};
-      if (kb < k1) panel_quad<MODE>(a, kb, c, w);
-      int cn_at = 0x7fffffff;
-      while (true) {  // warp-uniform
-        // the next step's quad is in flight while this one is used
-        const int kbn = kb + 4 * (32 / G);
+      if (j >= nl) continue;  // warp-uniform
+      const int ra = max(__shfl_sync(0xffffffffu, lo, j), W0);
+      const int rb = min(__shfl_sync(0xffffffffu, hi, j), W1);
+      for (int kb0 = ra & ~3; kb0 < rb; kb0 += STEP) {  // warp-uniform
+        const int kb = kb0 + 4 * grp;
+        if (pre != kb0 && kb < rb) panel_quad<MODE>(a, kb, c, w);
+        // the next step: further along this run, or the first step of the
+        // next non-empty run (later lines of this panel, then the next panel)
+        int nk = -1, nb = 0;
+        if (kb0 + STEP < rb) {
+          nk = kb0 + STEP;
+          nb = rb;
+        } else {
+          for (int jj = j + 1; jj < nl; ++jj) {
+            const int xa = max(__shfl_sync(0xffffffffu, lo, jj), W0);
+            const int xb = min(__shfl_sync(0xffffffffu, hi, jj), W1);
+            if (xb > xa) {
+              nk = xa & ~3;
+              nb = xb;
+              break;
+            }
+          }
+          if (nk < 0 && p + 1 < npanels) {
+            for (int jj = 0; jj < nl; ++jj) {
+              const int xa = max(__shfl_sync(0xffffffffu, hi, jj), W0);
+              const int xb = min(__shfl_sync(0xffffffffu, hh, jj), W1);
+              if (xb > xa) {
+                nk = xa & ~3;
+                nb = xb;
+                break;
+              }
+            }
+          }
+        }
         int cn[4] = {0, 0, 0, 0};
         float wn[4] = {0.f, 0.f, 0.f, 0.f};
-        if (kbn < k1) panel_quad<MODE>(a, kbn, cn, wn);
-        const int lo = k - kb, hi = k1 - kb;  // entry e is in range iff lo <= e < hi
+        if (nk >= 0 && nk + 4 * grp < nb) panel_quad<MODE>(a, nk + 4 * grp, cn, wn);
+
         bool t[4];
-        int cnt = 0;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          t[e] = e >= lo && e < hi && c[e] < pend;
-          cnt += t[e] ? 1 : 0;
-        }
+        for (int e = 0; e < 4; ++e) t[e] = kb + e >= ra && kb + e < rb;
         if constexpr (MODE == kPanelSddmm) {
           float d[4];
 #pragma unroll
@@ -417,39 +439,18 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
                     acc[j][v][i] = fmaf(w[e0 + e], x[e][v][i], acc[j][v][i]);
           }
         }
-        // The taken entries are a prefix of [k, k1) (a line's entries are
-        // sorted by operand index): advance past them; stop at the first
-        // entry of a later panel.
-        const int total = (int)(__reduce_add_sync(0xffffffffu, (unsigned)cnt) / G);
-        const int step_end = (k & ~3) + 4 * (32 / G);
-        const int in_step = min(k1, step_end) - k;
-        const int k_old = k;
-        k += total;
-        if (total < in_step) {
-          // operand index of the entry now at the cursor, from the group
-          // whose quad holds it
-          const int comp = k & 3;
-          const int mine = comp == 0 ? c[0] : comp == 1 ? c[1] : comp == 2 ? c[2] : c[3];
-          cn_at = __shfl_sync(0xffffffffu, mine, ((k - (k_old & ~3)) >> 2) * G);
-          break;
-        }
-        if (k >= k1) break;
-        kb = kbn;
+        pre = nk;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           c[e] = cn[e];
           w[e] = wn[e];
         }
       }
-      __syncwarp();
-      if (lane == 0) {
-        cur[j] = k;
-        nxt[j] = cn_at;  // INT_MAX once the warp's part of the line is done
-      }
-      __syncwarp();
     }
     __syncwarp();
     if (lane == 0) bar_arrive(&empty[s]);
+    lo = hi;
+    hi = hh;
   }
   if constexpr (MODE != kPanelSddmm)
     panel_spmm_out<BW, RW>(a, acc, part, slot, warp, lane, nl, first, W0, W1);
@@ -487,6 +488,11 @@ cudaError_t launch_panel_kernel(K kern, const PanelArgs &a, int64_t ctas, size_t
 
 }  // namespace
 
+namespace {
+int width_index(int bw) { return bw == 8 ? 0 : bw == 16 ? 1 : bw == 32 ? 2 : 3; }
+int width_of(int i) { return 8 << i; }
+}  // namespace
+
 int64_t panel_min_nnz() {
   const char *e = std::getenv("SNACK_PANEL_MIN_NNZ");
   if (e && *e) {
@@ -499,13 +505,65 @@ int64_t panel_min_nnz() {
 
 bool panel_fits(const PanelTable &t, int bw) {
   return t.d_part != nullptr && t.lines_max <= kPanelLinesPerWarp &&
-         (bw == 8 || bw == 16 || bw == 32 || bw == 64);
+         (bw == 8 || bw == 16 || bw == 32 || bw == 64) && t.d_off[width_index(bw)] != nullptr;
+}
+
+namespace {
+// off[p][l] = first entry of line l (entries ptr[l] .. ptr[l+1], sorted by
+// operand index) whose operand index is at least p * pw.
+__global__ void panel_offsets(const int32_t *__restrict__ ptr, const int32_t *__restrict__ idx,
+                              int64_t lines, int npan, int pw, int32_t *__restrict__ off) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= lines * (int64_t)(npan + 1)) return;
+  const int p = (int)(t / lines);
+  const int64_t l = t - (int64_t)p * lines;
+  int lo = ptr[l], hi = ptr[l + 1];
+  if (p == 0) {
+    off[t] = lo;
+    return;
+  }
+  if (p == npan) {
+    off[t] = hi;
+    return;
+  }
+  const int key = p * pw;
+  while (lo < hi) {
+    const int mid = lo + (hi - lo) / 2;
+    if (idx[mid] < key) lo = mid + 1;
+    else hi = mid;
+  }
+  off[t] = lo;
+}
+}  // namespace
+
+cudaError_t build_panel_offsets(PanelTable &t, const int32_t *ptr, const int32_t *idx,
+                                int64_t lines, int64_t n_op, size_t *acct, cudaStream_t s) {
+  for (int i = 0; i < kPanelWidths; ++i) {
+    const int pw = kStageBytes / (4 * width_of(i));
+    const int64_t npan = (n_op + pw - 1) / pw;
+    const int64_t n = lines * (npan + 1);
+    cudaError_t e = dev_alloc(&t.d_off[i], (size_t)n, acct);
+    t.bytes += (size_t)n * 4;
+    if (e != cudaSuccess) return e;
+    panel_offsets<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ptr, idx, lines, (int)npan, pw,
+                                                              t.d_off[i]);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+void free_panel_table(PanelTable &t) {
+  if (t.d_part) cudaFree(t.d_part);
+  for (int32_t *&p : t.d_off)
+    if (p) cudaFree(p);
+  t = PanelTable();
 }
 
 cudaError_t launch_panel(int mode, int bw, const PanelTable &t, const PanelArgs &args, bool pdl,
                          cudaStream_t s) {
   PanelArgs a = args;
   a.part = t.d_part;
+  a.off = t.d_off[width_index(bw)];
   const size_t smem = (size_t)kStages * kStageBytes + (size_t)kConsumers * bw * 4;
 #define SNACK_PANEL(W)                                                                         \
   case W:                                                                                      \

@@ -43,10 +43,17 @@ constexpr int kOptNone = 0, kOptSgd = 1, kOptAdam = 2;  // optimizer kinds
 constexpr int kPanelLinesPerWarp = 4;  // lines one consumer warp can hold
 constexpr int kPanelSpmm = 0, kPanelSpmmPerm = 1, kPanelSddmm = 2;  // panel kernel modes
 
+constexpr int kPanelWidths = 4;  // slices of 8, 16, 32, 64 floats
+
 struct PanelTable {
   int4 *d_part = nullptr;  // [ctas][32]
   int64_t ctas = 0;
   int lines_max = 0;       // most lines any consumer warp covers
+  // Per slice width (8, 16, 32, 64): run offsets [P + 1][lines], where
+  // off[p][l] is the first entry of line l whose operand index is at least
+  // p * PW (PW = operand lines per panel), off[0] = line start, off[P] = end.
+  int32_t *d_off[kPanelWidths] = {nullptr, nullptr, nullptr, nullptr};
+  size_t bytes = 0;        // device bytes of the partition and the offsets
 };
 
 struct SegTable {
@@ -155,6 +162,8 @@ struct PanelArgs {
   float *dw;             // dW output (canonical order)
   int accumulate;        // dW: add to dw (batch slices after the first)
   int *err;              // the layer's device error flag
+  const int32_t *off;    // the table's run offsets for this width (set by the launcher)
+  int64_t lines;         // lines of the table (row stride of off)
 };
 
 // Kernel selection: batch slice width, lanes per entry group, lanes per segment.
@@ -194,6 +203,12 @@ cudaError_t launch_panel(int mode, int bw, const PanelTable &t, const PanelArgs 
                          cudaStream_t s);
 void build_panel_partition(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz, int ctas,
                            std::vector<int4> &part, int *lines_max);
+// Run offsets of every width for a table of `lines` lines over an operand of
+// n_op lines (ptr / idx: the table's line pointer and index stream on the
+// device).  Allocates t.d_off[*] (bytes added to *acct); asynchronous on s.
+cudaError_t build_panel_offsets(PanelTable &t, const int32_t *ptr, const int32_t *idx,
+                                int64_t lines, int64_t n_op, size_t *acct, cudaStream_t s);
+void free_panel_table(PanelTable &t);
 // Smallest layer (stored entries) that gets panel partitions: 2^21, or the
 // SNACK_PANEL_MIN_NNZ environment variable when set.
 int64_t panel_min_nnz();

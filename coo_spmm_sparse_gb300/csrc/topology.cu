@@ -402,19 +402,24 @@ snack_status finish_layout(Layer &L, const uint64_t *d_cell_key, cudaStream_t s,
   // Column-panel partitions of both tables (large layers only).
   for (int dir = 0; dir < 2; ++dir) {
     PanelTable &pt = dir == 0 ? L.csr.panel : L.csc.panel;
-    if (pt.d_part) cudaFree(pt.d_part);
-    pt = PanelTable();
+    free_panel_table(pt);
     if (n < panel_min_nnz() || n == 0) continue;
     std::vector<int4> part;
     int lines_max = 0;
     const int ctas = device_sms();
-    build_panel_partition(dir == 0 ? rp : cp, dir == 0 ? L.out : L.in, n, ctas, part, &lines_max);
+    const int64_t lines = dir == 0 ? L.out : L.in;
+    build_panel_partition(dir == 0 ? rp : cp, lines, n, ctas, part, &lines_max);
+    if (lines_max > kPanelLinesPerWarp) continue;  // too many lines per warp: no panels
     TRY_CUDA(dev_alloc(&pt.d_part, part.size(), &L.device_bytes));
     TRY_CUDA(cudaMemcpyAsync(pt.d_part, part.data(), part.size() * sizeof(int4),
                              cudaMemcpyHostToDevice, s));
+    TRY_CUDA(build_panel_offsets(pt, dir == 0 ? L.d_row_ptr : L.d_col_ptr,
+                                 dir == 0 ? L.d_col : L.d_csc_row, lines, dir == 0 ? L.in : L.out,
+                                 &L.device_bytes, s));
     TRY_CUDA(cudaStreamSynchronize(s));
     pt.ctas = ctas;
     pt.lines_max = lines_max;
+    pt.bytes += part.size() * sizeof(int4);
   }
   // Split workspace: partial slots and re-armed tickets (zero between calls).
   if (L.d_partial) cudaFree(L.d_partial);
@@ -848,9 +853,11 @@ void free_layer(Layer &L) {
                   L.d_csc_perm, L.d_col_ptr, L.csr.d_seg,     L.csr.d_split,   L.csc.d_seg,
                   L.csc.d_split, L.d_xt,     L.d_dyt,         L.d_partial,     L.d_counter,
                   L.d_err,     L.d_opt[0],  L.d_opt[1],
-                  L.d_gacc,    L.d_val_csc, L.csr.panel.d_part, L.csc.panel.d_part};
+                  L.d_gacc,    L.d_val_csc};
   for (void *p : ptrs)
     if (p) cudaFree(p);
+  free_panel_table(L.csr.panel);
+  free_panel_table(L.csc.panel);
   L = Layer();
 }
 
