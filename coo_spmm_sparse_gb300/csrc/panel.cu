@@ -564,6 +564,7 @@ cudaError_t launch_panel(int mode, int bw, const PanelTable &t, const PanelArgs 
   PanelArgs a = args;
   a.part = t.d_part;
   a.off = t.d_off[width_index(bw)];
+  a.lines = t.lines;
   const size_t smem = (size_t)kStages * kStageBytes + (size_t)kConsumers * bw * 4;
 #define SNACK_PANEL(W)                                                                         \
   case W:                                                                                      \

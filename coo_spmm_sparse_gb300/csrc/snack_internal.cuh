@@ -48,6 +48,7 @@ constexpr int kPanelWidths = 4;  // slices of 8, 16, 32, 64 floats
 struct PanelTable {
   int4 *d_part = nullptr;  // [ctas][32]
   int64_t ctas = 0;
+  int64_t lines = 0;       // lines of the table
   int lines_max = 0;       // most lines any consumer warp covers
   // Per slice width (8, 16, 32, 64): run offsets [P + 1][lines], where
   // off[p][l] is the first entry of line l whose operand index is at least

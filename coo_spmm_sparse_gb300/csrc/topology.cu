@@ -418,6 +418,7 @@ snack_status finish_layout(Layer &L, const uint64_t *d_cell_key, cudaStream_t s,
                                  &L.device_bytes, s));
     TRY_CUDA(cudaStreamSynchronize(s));
     pt.ctas = ctas;
+    pt.lines = lines;
     pt.lines_max = lines_max;
     pt.bytes += part.size() * sizeof(int4);
   }
