@@ -49,8 +49,8 @@ namespace snack {
 
 namespace {
 
-constexpr int kPanelThreads = 1024;
-constexpr int kConsumers = 31;          // warps 0-30 consume, warp 31 produces
+constexpr int kPanelThreads = 768;
+constexpr int kConsumers = 23;          // warps 0-22 consume, warp 23 produces
 constexpr int kStages = 3;
 constexpr int kStageBytes = 64 * 1024;  // one panel
 constexpr int kChunkBytes = 32 * 1024;  // bulk copies per panel are cut at this size
@@ -108,12 +108,14 @@ __host__ __device__ constexpr int panel_lines() {
   return kStageBytes / (4 * BW);
 }
 
-// Batch-slice shape of the panel kernels: G = BW / 4 lanes per entry, each
-// holding one 16-byte vector of the row (a 64-float row is read by 16 lanes
-// with one instruction: two rows per 512-byte access, no bank conflict).
+// Batch-slice shape of the panel kernels: G = BW / 8 lanes per entry, each
+// holding two 16-byte vectors (8 floats) of the row.  The per-step work of a
+// lane (stream loads, masks, addresses) is then spread over 8 floats of
+// every entry instead of 4: fewer instructions per entry, one warp step
+// covering 128 / 64 / 32 / 16 entries at slices of 8 / 16 / 32 / 64.
 template <int BW>
 struct PanelShape {
-  static constexpr int VEC = 4, NV = 1, G = BW / 4;
+  static constexpr int VEC = 4, NV = 2, G = BW / 8;
 };
 
 // One quad (entries kb..kb+3) of the index / value streams.
@@ -146,11 +148,30 @@ __device__ __forceinline__ void panel_quad(const PanelArgs &a, int kb, int (&c)[
 // G = 2 / 4 / 8 / 16 the group spends 2 / 3 / 4 / 5 shuffles on its four
 // entries, and lane sub ends with entry (sub / (G / 4)) when G >= 4 (of
 // those, the lanes with sub % (G / 4) == 0 store it), or, for G = 2, with
-// entries 2 sub and 2 sub + 1.
+// entries 2 sub and 2 sub + 1.  With G = 1 the lane has the sums already.
 template <int G>
 __device__ __forceinline__ void panel_dw_store(const PanelArgs &a, int kb, int sub,
                                                const bool (&t)[4], float (&d)[4]) {
   const unsigned m = 0xffffffffu;
+  if constexpr (G == 1) {  // the lane holds whole dot products
+    float *dst = a.dw + kb;
+    if (t[0] && t[1] && t[2] && t[3]) {
+      float4 o = make_float4(d[0], d[1], d[2], d[3]);
+      if (a.accumulate) {
+        const float4 old = *reinterpret_cast<const float4 *>(dst);
+        o.x += old.x;
+        o.y += old.y;
+        o.z += old.z;
+        o.w += old.w;
+      }
+      *reinterpret_cast<float4 *>(dst) = o;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (t[e]) dst[e] = a.accumulate ? dst[e] + d[e] : d[e];
+    }
+    return;
+  } else {
   const bool up = (sub & (G / 2)) != 0;  // level 1: keep entries 2-3 (up) or 0-1
   const float s0 = __shfl_xor_sync(m, up ? d[0] : d[2], G / 2);
   const float s1 = __shfl_xor_sync(m, up ? d[1] : d[3], G / 2);
@@ -174,6 +195,7 @@ __device__ __forceinline__ void panel_dw_store(const PanelArgs &a, int kb, int s
       float *dst = a.dw + kb + e;
       *dst = a.accumulate ? *dst + d[0] : d[0];
     }
+  }
   }
 }
 
@@ -340,7 +362,7 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
   int pre = -1;
   int c[4] = {0, 0, 0, 0};
   float w[4] = {0.f, 0.f, 0.f, 0.f};
-  constexpr int EB = 2;  // entries gathered together
+  constexpr int EB = 1;  // entries gathered together
   bool ok = true;
   for (int p = 0; p < npanels && ok; ++p) {
     const int s = p % kStages;
@@ -588,9 +610,11 @@ cudaError_t launch_panel(int mode, int bw, const PanelTable &t, const PanelArgs 
 }
 
 // Entry-balanced partition of a line table for the panel kernels: `ctas`
-// CTAs take row-aligned shares of about nnz / ctas entries; each CTA's 31
-// consumer warps split its share evenly.  Per CTA 32 int4: warps 0-30
-// {first entry, end entry, first line, lines}, then {first line, end line}.
+// CTAs take row-aligned shares of about nnz / ctas entries; each CTA's
+// consumer warps split its share evenly, except that a warp's range is cut
+// at the start of its (kPanelLinesPerWarp + 1)-th line (the next warps take
+// the rest).  Per CTA 32 int4: one per consumer warp {first entry, end
+// entry, first line, lines}, then {first line, end line} of the CTA.
 void build_panel_partition(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz,
                            int ctas, std::vector<int4> &part, int *lines_max) {
   part.assign((size_t)ctas * 32, make_int4(0, 0, 0, 0));
@@ -610,15 +634,21 @@ void build_panel_partition(const std::vector<int32_t> &ptr, int64_t nlines, int6
       if (r1 < r0) r1 = r0;
     }
     const int64_t e0 = ptr[r0], e1 = ptr[r1];
+    int64_t w0 = e0;
     for (int w = 0; w < kConsumers; ++w) {
-      const int64_t w0 = e0 + (e1 - e0) * w / kConsumers;
-      const int64_t w1 = e0 + (e1 - e0) * (w + 1) / kConsumers;
+      // ideal end of the warp's share; cut earlier if the range would cover
+      // more lines than a warp holds (the following warps take the rest)
+      int64_t w1 = w + 1 == kConsumers ? e1 : e0 + (e1 - e0) * (w + 1) / kConsumers;
+      if (w1 < w0) w1 = w0;
       int first = (int)r0, n = 0;
       if (w1 > w0) {
         // line holding entry w0 (the last line starting at or before it
-        // whose range is not empty) and line holding entry w1 - 1
+        // whose range is not empty)
         const int64_t fa =
             std::upper_bound(ptr.begin() + r0, ptr.begin() + r1 + 1, (int32_t)w0) - ptr.begin() - 1;
+        if (fa + kPanelLinesPerWarp < r1 && ptr[fa + kPanelLinesPerWarp] < w1 &&
+            w + 1 < kConsumers)
+          w1 = ptr[fa + kPanelLinesPerWarp];
         const int64_t la = std::upper_bound(ptr.begin() + r0, ptr.begin() + r1 + 1,
                                             (int32_t)(w1 - 1)) -
                            ptr.begin() - 1;
@@ -627,6 +657,7 @@ void build_panel_partition(const std::vector<int32_t> &ptr, int64_t nlines, int6
       }
       part[(size_t)c * 32 + w] = make_int4((int)w0, (int)w1, first, n);
       *lines_max = std::max(*lines_max, n);
+      w0 = w1;
     }
     part[(size_t)c * 32 + kConsumers] = make_int4((int)r0, (int)r1, 0, 0);
     r0 = r1;
