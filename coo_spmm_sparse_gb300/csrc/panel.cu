@@ -108,14 +108,18 @@ __host__ __device__ constexpr int panel_lines() {
   return kStageBytes / (4 * BW);
 }
 
-// Batch-slice shape of the panel kernels: G = BW / 8 lanes per entry, each
-// holding two 16-byte vectors (8 floats) of the row.  The per-step work of a
-// lane (stream loads, masks, addresses) is then spread over 8 floats of
-// every entry instead of 4: fewer instructions per entry, one warp step
-// covering 128 / 64 / 32 / 16 entries at slices of 8 / 16 / 32 / 64.
+// Batch-slice shape of the panel kernels: G lanes per entry, each holding
+// NV 16-byte vectors of the row, QPS quads (4 entries each) per group per
+// step.  A warp's shared-memory gathers cost the most bank conflicts when a
+// lane reads part of a short row, so rows of up to 128 bytes are read whole
+// by one instruction of their group (G = BW / 4), and the per-step work of
+// a lane (stream loads, masks, addresses) is spread over two quads instead;
+// 64-float rows are read as two 128-byte halves (one vector per lane each,
+// conflict-free), one quad per step.
 template <int BW>
 struct PanelShape {
-  static constexpr int VEC = 4, NV = 2, G = BW / 8;
+  static constexpr int VEC = 4, NV = BW == 64 ? 2 : 1, G = BW == 64 ? 8 : BW / 4;
+  static constexpr int QPS = BW == 64 ? 1 : 2;
 };
 
 // One quad (entries kb..kb+3) of the index / value streams.
@@ -263,7 +267,7 @@ __device__ __forceinline__ void panel_spmm_out(const PanelArgs &a,
 template <int BW, int RW, int MODE>
 __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs a) {
   using S = PanelShape<BW>;
-  constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
+  constexpr int VEC = S::VEC, NV = S::NV, G = S::G, QPS = S::QPS;
   constexpr int PW = panel_lines<BW>();
   static_assert(PW * BW * 4 == kStageBytes, "panel size");
 
@@ -330,7 +334,8 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
 
   // ------------------------------------------------------------ consumers
   const int grp = lane / G, sub = lane % G;
-  constexpr int STEP = 4 * (32 / G);  // entries per warp step
+  constexpr int NPT = 32 / G;            // groups per warp
+  constexpr int STEP = 4 * NPT * QPS;    // entries per warp step
   const int4 me = part[warp];
   const int W0 = me.x, W1 = me.y, first = me.z, nl = me.w;
   // Run offsets of line j (lane j < RW holds them): lo = its first entry
@@ -358,10 +363,11 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
     }
   }
 
-  // The quad of the step at pre (a step base, multiple of 4), loaded ahead.
+  // The quads of the step based at pre (a multiple of 4), loaded ahead: this
+  // group's quad q starts at pre + 4 grp + 4 NPT q.
   int pre = -1;
-  int c[4] = {0, 0, 0, 0};
-  float w[4] = {0.f, 0.f, 0.f, 0.f};
+  int c[QPS][4] = {};
+  float w[QPS][4] = {};
   constexpr int EB = 1;  // entries gathered together
   bool ok = true;
   for (int p = 0; p < npanels && ok; ++p) {
@@ -382,7 +388,11 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
       const int rb = min(__shfl_sync(0xffffffffu, hi, j), W1);
       for (int kb0 = ra & ~3; kb0 < rb; kb0 += STEP) {  // warp-uniform
         const int kb = kb0 + 4 * grp;
-        if (pre != kb0 && kb < rb) panel_quad<MODE>(a, kb, c, w);
+        if (pre != kb0) {
+#pragma unroll
+          for (int q = 0; q < QPS; ++q)
+            if (kb + 4 * NPT * q < rb) panel_quad<MODE>(a, kb + 4 * NPT * q, c[q], w[q]);
+        }
         // the next step: further along this run, or the first step of the
         // next non-empty run (later lines of this panel, then the next panel)
         int nk = -1, nb = 0;
@@ -411,62 +421,74 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
             }
           }
         }
-        int cn[4] = {0, 0, 0, 0};
-        float wn[4] = {0.f, 0.f, 0.f, 0.f};
-        if (nk >= 0 && nk + 4 * grp < nb) panel_quad<MODE>(a, nk + 4 * grp, cn, wn);
-
-        bool t[4];
+        int cn[QPS][4] = {};
+        float wn[QPS][4] = {};
+        if (nk >= 0) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) t[e] = kb + e >= ra && kb + e < rb;
-        if constexpr (MODE == kPanelSddmm) {
-          float d[4];
-#pragma unroll
-          for (int e0 = 0; e0 < 4; e0 += EB) {
-            float x[EB][NV][VEC];
-#pragma unroll
-            for (int e = 0; e < EB; ++e)
-              if (t[e0 + e])
-#pragma unroll
-                for (int v = 0; v < NV; ++v)
-                  load_op<VEC, true>(st + c[e0 + e] * BW + v * G * VEC, x[e][v]);
-#pragma unroll
-            for (int e = 0; e < EB; ++e) {
-              float q = 0.f;
-              if (t[e0 + e])
-#pragma unroll
-                for (int v = 0; v < NV; ++v)
-#pragma unroll
-                  for (int i = 0; i < VEC; ++i) q = fmaf(acc[j][v][i], x[e][v][i], q);
-              d[e0 + e] = q;
-            }
+          for (int q = 0; q < QPS; ++q) {
+            const int kq = nk + 4 * grp + 4 * NPT * q;
+            if (kq < nb) panel_quad<MODE>(a, kq, cn[q], wn[q]);
           }
-          panel_dw_store<G>(a, kb, sub, t, d);
-        } else {
+        }
+
 #pragma unroll
-          for (int e0 = 0; e0 < 4; e0 += EB) {
-            float x[EB][NV][VEC];
+        for (int q = 0; q < QPS; ++q) {
+          const int kq = kb + 4 * NPT * q;
+          bool t[4];
 #pragma unroll
-            for (int e = 0; e < EB; ++e)
-              if (t[e0 + e])
+          for (int e = 0; e < 4; ++e) t[e] = kq + e >= ra && kq + e < rb;
+          if constexpr (MODE == kPanelSddmm) {
+            float d[4];
 #pragma unroll
-                for (int v = 0; v < NV; ++v)
-                  load_op<VEC, true>(st + c[e0 + e] * BW + v * G * VEC, x[e][v]);
+            for (int e0 = 0; e0 < 4; e0 += EB) {
+              float x[EB][NV][VEC];
 #pragma unroll
-            for (int e = 0; e < EB; ++e)
-              if (t[e0 + e])
+              for (int e = 0; e < EB; ++e)
+                if (t[e0 + e])
 #pragma unroll
-                for (int v = 0; v < NV; ++v)
+                  for (int v = 0; v < NV; ++v)
+                    load_op<VEC, true>(st + c[q][e0 + e] * BW + v * G * VEC, x[e][v]);
 #pragma unroll
-                  for (int i = 0; i < VEC; ++i)
-                    acc[j][v][i] = fmaf(w[e0 + e], x[e][v][i], acc[j][v][i]);
+              for (int e = 0; e < EB; ++e) {
+                float dot = 0.f;
+                if (t[e0 + e])
+#pragma unroll
+                  for (int v = 0; v < NV; ++v)
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) dot = fmaf(acc[j][v][i], x[e][v][i], dot);
+                d[e0 + e] = dot;
+              }
+            }
+            panel_dw_store<G>(a, kq, sub, t, d);
+          } else {
+#pragma unroll
+            for (int e0 = 0; e0 < 4; e0 += EB) {
+              float x[EB][NV][VEC];
+#pragma unroll
+              for (int e = 0; e < EB; ++e)
+                if (t[e0 + e])
+#pragma unroll
+                  for (int v = 0; v < NV; ++v)
+                    load_op<VEC, true>(st + c[q][e0 + e] * BW + v * G * VEC, x[e][v]);
+#pragma unroll
+              for (int e = 0; e < EB; ++e)
+                if (t[e0 + e])
+#pragma unroll
+                  for (int v = 0; v < NV; ++v)
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i)
+                      acc[j][v][i] = fmaf(w[q][e0 + e], x[e][v][i], acc[j][v][i]);
+            }
           }
         }
         pre = nk;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          c[e] = cn[e];
-          w[e] = wn[e];
-        }
+        for (int q = 0; q < QPS; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            c[q][e] = cn[q][e];
+            w[q][e] = wn[q][e];
+          }
       }
     }
     __syncwarp();
