@@ -119,7 +119,7 @@ __host__ __device__ constexpr int panel_lines() {
 template <int BW>
 struct PanelShape {
   static constexpr int VEC = 4, NV = BW == 64 ? 2 : 1, G = BW == 64 ? 8 : BW / 4;
-  static constexpr int QPS = 1;
+  static constexpr int QPS = BW == 64 ? 1 : 2;
 };
 
 // One quad (entries kb..kb+3) of the index / value streams.
@@ -273,14 +273,12 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
 
   extern __shared__ __align__(128) float smem_f[];
   float *stage = smem_f;                                  // [kStages][PW][BW]
-  float *zrow = smem_f + kStages * PW * BW;               // one row of zeros (masked gathers)
-  float *slot = zrow + BW;                                // [kConsumers][BW]
+  float *slot = smem_f + kStages * PW * BW;               // [kConsumers][BW]
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
   __shared__ int4 part[32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid < 32) part[tid] = a.part[(int64_t)blockIdx.x * 32 + tid];
-  if (tid < BW) zrow[tid] = 0.f;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&full[s])), "r"(1)
@@ -370,6 +368,7 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
   int pre = -1;
   int c[QPS][4] = {};
   float w[QPS][4] = {};
+  constexpr int EB = 1;  // entries gathered together
   bool ok = true;
   for (int p = 0; p < npanels && ok; ++p) {
     const int s = p % kStages;
@@ -432,10 +431,6 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
           }
         }
 
-        // Masked entries (outside the run) gather the zero row with a zero
-        // weight: no branches, and they add exactly nothing even when a
-        // value or an operand row holds an infinity or a NaN.
-        const float *zr = zrow + sub * VEC;
 #pragma unroll
         for (int q = 0; q < QPS; ++q) {
           const int kq = kb + 4 * NPT * q;
@@ -445,31 +440,44 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
           if constexpr (MODE == kPanelSddmm) {
             float d[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float *row = t[e] ? st + c[q][e] * BW : zr;
-              float x[NV][VEC];
+            for (int e0 = 0; e0 < 4; e0 += EB) {
+              float x[EB][NV][VEC];
 #pragma unroll
-              for (int v = 0; v < NV; ++v) load_op<VEC, true>(row + v * G * VEC, x[v]);
-              float dot = 0.f;
+              for (int e = 0; e < EB; ++e)
+                if (t[e0 + e])
 #pragma unroll
-              for (int v = 0; v < NV; ++v)
+                  for (int v = 0; v < NV; ++v)
+                    load_op<VEC, true>(st + c[q][e0 + e] * BW + v * G * VEC, x[e][v]);
 #pragma unroll
-                for (int i = 0; i < VEC; ++i) dot = fmaf(acc[j][v][i], x[v][i], dot);
-              d[e] = dot;
+              for (int e = 0; e < EB; ++e) {
+                float dot = 0.f;
+                if (t[e0 + e])
+#pragma unroll
+                  for (int v = 0; v < NV; ++v)
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) dot = fmaf(acc[j][v][i], x[e][v][i], dot);
+                d[e0 + e] = dot;
+              }
             }
             panel_dw_store<G>(a, kq, sub, t, d);
           } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float *row = t[e] ? st + c[q][e] * BW : zr;
-              const float we = t[e] ? w[q][e] : 0.f;
-              float x[NV][VEC];
+            for (int e0 = 0; e0 < 4; e0 += EB) {
+              float x[EB][NV][VEC];
 #pragma unroll
-              for (int v = 0; v < NV; ++v) load_op<VEC, true>(row + v * G * VEC, x[v]);
+              for (int e = 0; e < EB; ++e)
+                if (t[e0 + e])
 #pragma unroll
-              for (int v = 0; v < NV; ++v)
+                  for (int v = 0; v < NV; ++v)
+                    load_op<VEC, true>(st + c[q][e0 + e] * BW + v * G * VEC, x[e][v]);
 #pragma unroll
-                for (int i = 0; i < VEC; ++i) acc[j][v][i] = fmaf(we, x[v][i], acc[j][v][i]);
+              for (int e = 0; e < EB; ++e)
+                if (t[e0 + e])
+#pragma unroll
+                  for (int v = 0; v < NV; ++v)
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i)
+                      acc[j][v][i] = fmaf(w[q][e0 + e], x[e][v][i], acc[j][v][i]);
             }
           }
         }
@@ -601,7 +609,7 @@ cudaError_t launch_panel(int mode, int bw, const PanelTable &t, const PanelArgs 
   a.part = t.d_part;
   a.off = t.d_off[width_index(bw)];
   a.lines = t.lines;
-  const size_t smem = (size_t)kStages * kStageBytes + (size_t)(kConsumers + 1) * bw * 4;
+  const size_t smem = (size_t)kStages * kStageBytes + (size_t)kConsumers * bw * 4;
 #define SNACK_PANEL(W)                                                                         \
   case W:                                                                                      \
     if (mode == kPanelSpmm)                                                                    \
