@@ -165,22 +165,6 @@ cudaError_t launch_cols(const snack::Layer &L, const snack::Plan &p, snack::Spmm
   return a.perm ? snack::launch_spmm_cols(q, a, true, s) : snack::launch_spmm_rows(q, a, true, s);
 }
 
-// Column-panel launch arguments of one direction (rows: the forward and
-// dW, operand X^T; columns: dX, operand dY^T).
-snack::PanelArgs panel_args(snack::Layer &L, bool rows, const float *op, int nb) {
-  snack::PanelArgs a = {};
-  a.ptr = rows ? L.d_row_ptr : L.d_col_ptr;
-  a.idx = rows ? L.d_col : L.d_csc_row;
-  a.val = rows || !L.csc_vals ? L.d_val : L.d_val_csc;
-  a.perm = rows ? nullptr : L.d_csc_perm;
-  a.src = op;
-  a.n_op = rows ? L.in : L.out;
-  a.ld = rows ? L.out : L.in;
-  a.nb = nb;
-  a.err = L.d_err;
-  return a;
-}
-
 // Forward Y = X W^T over batch slices of at most 256: the slice of X is
 // transposed into the workspace (not needed for a single row), then the
 // row-segment kernel runs.  Every launch is a programmatic dependent of the
@@ -201,14 +185,6 @@ snack_status run_forward(snack_handle h, const float *X, float *Y, int64_t batch
       op = L.d_xt;
     }
     cudaError_t e;
-    if (snack::panel_fits(L.csr.panel, p.bw)) {
-      snack::PanelArgs pa = panel_args(L, true, op, nb);
-      pa.dst = Y + b0 * L.out;
-      e = snack::launch_panel(snack::kPanelSpmm, p.bw, L.csr.panel, pa, true, s);
-      if (e != cudaSuccess) return cuda_fail(h, e, "forward launch");
-      g_launches.fetch_add(1, std::memory_order_relaxed);
-      continue;
-    }
     snack::SpmmArgs a = spmm_args(L, true, op, Y + b0 * L.out, nb);
     a.prefetch = transposed;
     a.stride = p.bw;
@@ -272,37 +248,29 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     if (opt) rows.opt = *opt;
   }
   cudaError_t e;
-  const bool pan_c = dX && snack::panel_fits(L.csc.panel, pc.bw);
-  const bool pan_r = want_w && !fused_opt && snack::panel_fits(L.csr.panel, pr.bw);
-  if (pan_c || pan_r) {
-    // Column-panel kernels for at least one product: one launch per product,
-    // the second a programmatic dependent of the first.
+  const bool pan_r =
+      want_w && !fused_opt && snack::panel_fits(L.csr.panel, pr.bw, L.csr.mean_len, L.in);
+  if (pan_r) {
+    // The weight product as a column-panel sweep (long rows): dX, when asked
+    // for, in its own launch first, then the sweep as its dependent.
     if (dX) {
-      if (pan_c) {
-        snack::PanelArgs pa = panel_args(L, false, dyt, nb);
-        pa.dst = dX + b0 * L.in;
-        e = snack::launch_panel(L.csc_vals ? snack::kPanelSpmm : snack::kPanelSpmmPerm, pc.bw,
-                                L.csc.panel, pa, true, s);
-      } else {
-        e = launch_cols(L, pc, cols, nb, s);
-      }
+      e = snack::resident_fits(pc.bw, L.out, L.csc.nseg, L.nnz)
+              ? snack::launch_resident_spmm(cols.perm != nullptr, pc, cols, L.out, L.d_err, true, s)
+              : launch_cols(L, pc, cols, nb, s);
       if (e != cudaSuccess) return cuda_fail(h, e, "backward-input launch");
       g_launches.fetch_add(1, std::memory_order_relaxed);
     }
-    if (want_w) {
-      if (pan_r) {
-        snack::PanelArgs pa = panel_args(L, true, xt, nb);
-        pa.dyt = dyt;
-        pa.dw = dW;
-        pa.accumulate = b0 > 0;
-        e = snack::launch_panel(snack::kPanelSddmm, pr.bw, L.csr.panel, pa, true, s);
-      } else {
-        rows.nsub = sddmm_subranges(L.csr, pr);
-        e = snack::launch_sddmm(pr, rows, true, s);
-      }
-      if (e != cudaSuccess) return cuda_fail(h, e, "backward-weight launch");
-      g_launches.fetch_add(1, std::memory_order_relaxed);
-    }
+    snack::PanelArgs pa = {};
+    pa.idx = L.d_col;
+    pa.src = xt;
+    pa.n_op = L.in;
+    pa.dyt = dyt;
+    pa.dw = dW;
+    pa.accumulate = b0 > 0;
+    pa.err = L.d_err;
+    e = snack::launch_panel_sddmm(pr.bw, L.csr.panel, pa, true, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "backward-weight launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return SNACK_OK;
   }
   const bool res_c = dX && snack::resident_fits(pc.bw, L.out, L.csc.nseg, L.nnz);
@@ -745,7 +713,7 @@ snack_status snack_plan(snack_handle h, int op, int64_t batch, int32_t *slice_wi
   if (lanes_per_segment) *lanes_per_segment = p.lanes;
   if (segments) *segments = t.nseg;
   if (resident)
-    *resident = snack::panel_fits(t.panel, p.bw)
+    *resident = op == 2 && snack::panel_fits(t.panel, p.bw, t.mean_len, h->L.in)
                     ? 2
                     : (snack::resident_fits(p.bw, op == 1 ? h->L.out : h->L.in, t.nseg, h->L.nnz)
                            ? 1

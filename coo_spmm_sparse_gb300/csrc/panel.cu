@@ -1,42 +1,43 @@
-// Column-panel kernels: the dense operand staged in shared memory panel by
-// panel, for batch slices of 8-64 floats.
+// Column-panel SDDMM: the backward-weight product dW[k] = sum_b dY[b][row_k]
+// X[b][col_k] with X^T staged in shared memory panel by panel, for batch
+// slices of 8-64 floats on layers whose rows are long.
 //
-// At slices of 8+ floats the segment kernels gather every entry's operand
-// row (32-256 bytes) through L1, and the L1 data pipe (one wavefront per
-// gathered row) with the L2 misses behind it sets their time.  Here each
-// CTA (one per SM, 1024 threads) sweeps the transposed operand [n_op][BW]
-// through shared memory in column panels of PW = 64 KB / (4 BW) lines,
-// three panels resident at a time:
+// The segment kernels gather every entry's X^T row (32-256 bytes) through
+// L1.  Here each CTA (one per SM, 768 threads) sweeps X^T [in][BW] through
+// shared memory in column panels of PW = 64 KB / (4 BW) lines, three panels
+// resident at a time:
 //
-//  * warp 31 is the producer: its lane 0 copies panel p into stage p % 3
+//  * warp 23 is the producer: its lane 0 copies panel p into stage p % 3
 //    with cp.async.bulk (completion on that stage's "full" mbarrier) once
-//    all 31 consumer warps have released the panel that stage held (its
+//    all 23 consumer warps have released the panel that stage held (its
 //    "empty" mbarrier).  Every wait is bounded; a wait that gives up sets
 //    the layer's device error flag and the CTA winds down.
-//  * each consumer warp owns a contiguous range of the line-ordered entry
-//    stream (the CTA's lines are a row-aligned, entry-balanced share of the
-//    table; its 31 warps split that share evenly), covering at most RW
-//    lines.  Entries of a line are sorted by the operand index, so the part
-//    of a line that falls in panel p is one run of consecutive entries; a
-//    table built with the topology holds every line's run offsets for every
-//    panel.  For each resident panel the warp walks its lines' runs in steps
-//    of one quad (4 entries) per group of G lanes, gathering the operand rows
-//    from shared memory.  Every step's address is known in advance (the next
-//    quad of the run, or the first of the next non-empty run, in this panel
-//    or the next), so the next step's index / value loads are always in
-//    flight while the current step gathers.
-//  * forward / dX: the lines' sums stay in registers across all panels.  At
-//    the end each warp reduces them over its groups; lines wholly inside a
-//    warp's range are written directly, a line cut by warp boundaries is
-//    summed by the warp where it starts, adding the other warps' parts in
-//    warp order through shared memory (deterministic, no atomics).
-//  * dW: the line's dY slice stays in registers; each entry's dot product
-//    is finished by a shuffle reduction over its group and stored.
+//  * each consumer warp owns a contiguous range of the row-ordered entry
+//    stream (the CTA's rows are a row-aligned, entry-balanced share of the
+//    table; its 23 warps split that share evenly, at most four rows each).
+//    Entries of a row are sorted by column, so the part of a row that falls
+//    in panel p is one run of consecutive entries; a table built with the
+//    topology holds every row's run offsets for every panel.  For each
+//    resident panel the warp walks its rows' runs in steps of two quads (4
+//    entries each) per group of G lanes, gathering X^T rows from shared
+//    memory; the rows' dY slices stay in registers, and each entry's dot
+//    product is finished by a butterfly over its group and stored.  Every
+//    step's address is known in advance (the next quads of the run, or the
+//    first of the next non-empty run, in this panel or the next), so the
+//    next step's index loads are always in flight.
 //
-// The index and value streams of the warp's range are asked into L2 at the
-// start (cp.async.bulk.prefetch.L2, before the wait on the producing
-// transpose): the sweep reads each line's runs panel by panel, not in one
-// pass, and L2 hits keep those short runs cheap.
+// It pays when a row's run per panel is long (a step covers 64 / 32 / 16 /
+// 16 entries at slices of 8 / 16 / 32 / 64): measured on GB300 against the
+// segment SDDMM, 10000 x 10000 at 90 % (1000 entries per row) batch 8 / 16 /
+// 32: 41.5 / 63.9 / 118.3 us vs 48.3 / 71.2 / 123.5; at 95 % batch 8: 27.9
+// vs 31.3, batch 16: 43.0 vs 41.5.  The launcher takes it when the mean run
+// per panel is at least 64 entries.  (The same sweep for the forward and dX
+// products measured slower than the segment kernels at every width.)
+//
+// The index stream of the warp's range is asked into L2 at the start
+// (cp.async.bulk.prefetch.L2, before the wait on the producing transpose):
+// the sweep reads each row's runs panel by panel, not in one pass, and L2
+// hits keep those short runs cheap.
 #include <algorithm>
 #include <cstdlib>
 #include <map>
@@ -98,11 +99,6 @@ __device__ __forceinline__ void load_panel(const float *src, int64_t first_line,
   }
 }
 
-// Consumer-warp barrier (named barrier 1, the 31 consumer warps only).
-__device__ __forceinline__ void consumers_sync() {
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
-}
-
 template <int BW>
 __host__ __device__ constexpr int panel_lines() {
   return kStageBytes / (4 * BW);
@@ -122,27 +118,13 @@ struct PanelShape {
   static constexpr int QPS = BW == 64 ? 1 : 2;
 };
 
-// One quad (entries kb..kb+3) of the index / value streams.
-template <int MODE>
-__device__ __forceinline__ void panel_quad(const PanelArgs &a, int kb, int (&c)[4], float (&w)[4]) {
+// Operand indices of one quad (entries kb..kb+3).
+__device__ __forceinline__ void panel_quad(const PanelArgs &a, int kb, int (&c)[4]) {
   const int4 c4 = ld_stream_i4(a.idx + kb);
   c[0] = c4.x;
   c[1] = c4.y;
   c[2] = c4.z;
   c[3] = c4.w;
-  if constexpr (MODE == kPanelSpmm) {
-    const float4 v4 = ld_stream_f4(a.val + kb);
-    w[0] = v4.x;
-    w[1] = v4.y;
-    w[2] = v4.z;
-    w[3] = v4.w;
-  } else if constexpr (MODE == kPanelSpmmPerm) {
-    const int4 p4 = ld_stream_i4(a.perm + kb);
-    w[0] = __ldg(a.val + p4.x);
-    w[1] = __ldg(a.val + p4.y);
-    w[2] = __ldg(a.val + p4.z);
-    w[3] = __ldg(a.val + p4.w);
-  }
 }
 
 // dW of one quad: d[e] holds each lane's part of entry e's dot product
@@ -203,77 +185,15 @@ __device__ __forceinline__ void panel_dw_store(const PanelArgs &a, int kb, int s
   }
 }
 
-// Forward / dX epilogue of a consumer warp: reduce the lines' sums over the
-// groups, then write them out.  A line that starts in this warp's range is
-// this warp's to write; its parts in later warps (a line cut by warp
-// boundaries) arrive through `slot`, added in warp order.  Lines without
-// entries get zeros.
 template <int BW, int RW>
-__device__ __forceinline__ void panel_spmm_out(const PanelArgs &a,
-                                               float (&acc)[RW][PanelShape<BW>::NV]
-                                                           [PanelShape<BW>::VEC],
-                                               const int4 *part, float *slot, int warp, int lane,
-                                               int nl, int first, int W0, int W1) {
-  using S = PanelShape<BW>;
-  constexpr int VEC = S::VEC, NV = S::NV, G = S::G;
-  const int grp = lane / G, sub = lane % G;
-#pragma unroll
-  for (int j = 0; j < RW; ++j)
-#pragma unroll
-    for (int off = G; off < 32; off <<= 1)
-#pragma unroll
-      for (int v = 0; v < NV; ++v)
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) acc[j][v][i] += __shfl_xor_sync(0xffffffffu, acc[j][v][i], off);
-  const bool head_cut = nl > 0 && a.ptr[first] < W0;  // first line started in an earlier warp
-  if (head_cut && grp == 0) {
-#pragma unroll
-    for (int v = 0; v < NV; ++v)
-#pragma unroll
-      for (int i = 0; i < VEC; ++i) slot[warp * BW + v * G * VEC + sub * VEC + i] = acc[0][v][i];
-  }
-  consumers_sync();
-  const int4 cta = part[kConsumers];  // {first line, end line} of this CTA
-#pragma unroll
-  for (int j = 0; j < RW; ++j) {
-    if (j >= nl || (j == 0 && head_cut)) continue;
-    const int r = first + j;
-    const int rend = a.ptr[r + 1];
-    if (rend > W1) {  // cut: add the later warps' parts in order
-      for (int w2 = warp + 1; w2 < kConsumers && part[w2].x < rend; ++w2) {
-        if (part[w2].y <= part[w2].x) continue;
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-#pragma unroll
-          for (int i = 0; i < VEC; ++i) acc[j][v][i] += slot[w2 * BW + v * G * VEC + sub * VEC + i];
-      }
-    }
-    if (grp == 0) {
-#pragma unroll
-      for (int v = 0; v < NV; ++v)
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) {
-          const int b = v * G * VEC + sub * VEC + i;
-          if (b < a.nb) a.dst[(int64_t)b * a.ld + r] = acc[j][v][i];
-        }
-    }
-  }
-  for (int r = cta.x + warp * 32 + lane; r < cta.y; r += kConsumers * 32) {
-    if (a.ptr[r] == a.ptr[r + 1])
-      for (int b = 0; b < a.nb; ++b) a.dst[(int64_t)b * a.ld + r] = 0.f;
-  }
-}
-
-template <int BW, int RW, int MODE>
-__global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs a) {
+__global__ void __launch_bounds__(kPanelThreads, 1) panel_sddmm(const PanelArgs a) {
   using S = PanelShape<BW>;
   constexpr int VEC = S::VEC, NV = S::NV, G = S::G, QPS = S::QPS;
   constexpr int PW = panel_lines<BW>();
   static_assert(PW * BW * 4 == kStageBytes, "panel size");
 
   extern __shared__ __align__(128) float smem_f[];
-  float *stage = smem_f;                                  // [kStages][PW][BW]
-  float *slot = smem_f + kStages * PW * BW;               // [kConsumers][BW]
+  float *stage = smem_f;  // [kStages][PW][BW]
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
   __shared__ int4 part[32];
 
@@ -290,16 +210,12 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  // The warp's index / value streams are immutable here: ask L2 for them
-  // while the producing transpose may still run.
+  // The warp's index stream is immutable here: ask L2 for it while the
+  // producing transpose may still run.
   if (warp < kConsumers && lane == 0) {
     const int4 me = part[warp];
     const int k0 = me.x & ~3, k1 = (me.y + 3) & ~3;
-    if (k1 > k0) {
-      l2_prefetch(a.idx + k0, (uint32_t)(k1 - k0) * 4);
-      if (MODE == kPanelSpmmPerm) l2_prefetch(a.perm + k0, (uint32_t)(k1 - k0) * 4);
-      else if (MODE == kPanelSpmm) l2_prefetch(a.val + k0, (uint32_t)(k1 - k0) * 4);
-    }
+    if (k1 > k0) l2_prefetch(a.idx + k0, (uint32_t)(k1 - k0) * 4);
   }
   griddep_wait();
   const int npanels = (int)((a.n_op + PW - 1) / PW);
@@ -338,8 +254,8 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
   constexpr int STEP = 4 * NPT * QPS;    // entries per warp step
   const int4 me = part[warp];
   const int W0 = me.x, W1 = me.y, first = me.z, nl = me.w;
-  // Run offsets of line j (lane j < RW holds them): lo = its first entry
-  // in panel p, hi = first entry in panel p + 1, hh = in panel p + 2.
+  // Run offsets of row j (lane j < nl holds them): lo = its first entry in
+  // panel p, hi = first entry in panel p + 1, hh = in panel p + 2.
   const bool holder = lane < nl;
   const int32_t *offl = a.off + first + lane;
   int lo = 0, hi = 0, hh = 0;
@@ -347,19 +263,17 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
     lo = offl[0];
     hi = npanels >= 1 ? offl[(int64_t)a.lines] : lo;
   }
-  float acc[RW][NV][VEC];  // forward / dX: line sums; dW: the line's dY slice
+  float dy[RW][NV][VEC];  // each row's dY slice (the lane's part of the batch)
 #pragma unroll
   for (int j = 0; j < RW; ++j) {
 #pragma unroll
     for (int v = 0; v < NV; ++v)
 #pragma unroll
-      for (int i = 0; i < VEC; ++i) acc[j][v][i] = 0.f;
-    if constexpr (MODE == kPanelSddmm) {
-      if (j < nl) {
-        const float *p = a.dyt + (int64_t)(first + j) * BW + sub * VEC;
+      for (int i = 0; i < VEC; ++i) dy[j][v][i] = 0.f;
+    if (j < nl) {
+      const float *p = a.dyt + (int64_t)(first + j) * BW + sub * VEC;
 #pragma unroll
-        for (int v = 0; v < NV; ++v) load_vec<VEC>(p + v * G * VEC, acc[j][v]);
-      }
+      for (int v = 0; v < NV; ++v) load_vec<VEC>(p + v * G * VEC, dy[j][v]);
     }
   }
 
@@ -367,8 +281,6 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
   // group's quad q starts at pre + 4 grp + 4 NPT q.
   int pre = -1;
   int c[QPS][4] = {};
-  float w[QPS][4] = {};
-  constexpr int EB = 1;  // entries gathered together
   bool ok = true;
   for (int p = 0; p < npanels && ok; ++p) {
     const int s = p % kStages;
@@ -391,10 +303,10 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
         if (pre != kb0) {
 #pragma unroll
           for (int q = 0; q < QPS; ++q)
-            if (kb + 4 * NPT * q < rb) panel_quad<MODE>(a, kb + 4 * NPT * q, c[q], w[q]);
+            if (kb + 4 * NPT * q < rb) panel_quad(a, kb + 4 * NPT * q, c[q]);
         }
         // the next step: further along this run, or the first step of the
-        // next non-empty run (later lines of this panel, then the next panel)
+        // next non-empty run (later rows of this panel, then the next panel)
         int nk = -1, nb = 0;
         if (kb0 + STEP < rb) {
           nk = kb0 + STEP;
@@ -422,12 +334,11 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
           }
         }
         int cn[QPS][4] = {};
-        float wn[QPS][4] = {};
         if (nk >= 0) {
 #pragma unroll
           for (int q = 0; q < QPS; ++q) {
             const int kq = nk + 4 * grp + 4 * NPT * q;
-            if (kq < nb) panel_quad<MODE>(a, kq, cn[q], wn[q]);
+            if (kq < nb) panel_quad(a, kq, cn[q]);
           }
         }
 
@@ -437,58 +348,28 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
           bool t[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) t[e] = kq + e >= ra && kq + e < rb;
-          if constexpr (MODE == kPanelSddmm) {
-            float d[4];
+          float d[4];
 #pragma unroll
-            for (int e0 = 0; e0 < 4; e0 += EB) {
-              float x[EB][NV][VEC];
+          for (int e = 0; e < 4; ++e) {
+            float x[NV][VEC];
+            float dot = 0.f;
+            if (t[e]) {
 #pragma unroll
-              for (int e = 0; e < EB; ++e)
-                if (t[e0 + e])
+              for (int v = 0; v < NV; ++v) load_op<VEC, true>(st + c[q][e] * BW + v * G * VEC, x[v]);
 #pragma unroll
-                  for (int v = 0; v < NV; ++v)
-                    load_op<VEC, true>(st + c[q][e0 + e] * BW + v * G * VEC, x[e][v]);
+              for (int v = 0; v < NV; ++v)
 #pragma unroll
-              for (int e = 0; e < EB; ++e) {
-                float dot = 0.f;
-                if (t[e0 + e])
-#pragma unroll
-                  for (int v = 0; v < NV; ++v)
-#pragma unroll
-                    for (int i = 0; i < VEC; ++i) dot = fmaf(acc[j][v][i], x[e][v][i], dot);
-                d[e0 + e] = dot;
-              }
+                for (int i = 0; i < VEC; ++i) dot = fmaf(dy[j][v][i], x[v][i], dot);
             }
-            panel_dw_store<G>(a, kq, sub, t, d);
-          } else {
-#pragma unroll
-            for (int e0 = 0; e0 < 4; e0 += EB) {
-              float x[EB][NV][VEC];
-#pragma unroll
-              for (int e = 0; e < EB; ++e)
-                if (t[e0 + e])
-#pragma unroll
-                  for (int v = 0; v < NV; ++v)
-                    load_op<VEC, true>(st + c[q][e0 + e] * BW + v * G * VEC, x[e][v]);
-#pragma unroll
-              for (int e = 0; e < EB; ++e)
-                if (t[e0 + e])
-#pragma unroll
-                  for (int v = 0; v < NV; ++v)
-#pragma unroll
-                    for (int i = 0; i < VEC; ++i)
-                      acc[j][v][i] = fmaf(w[q][e0 + e], x[e][v][i], acc[j][v][i]);
-            }
+            d[e] = dot;
           }
+          panel_dw_store<G>(a, kq, sub, t, d);
         }
         pre = nk;
 #pragma unroll
         for (int q = 0; q < QPS; ++q)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            c[q][e] = cn[q][e];
-            w[q][e] = wn[q][e];
-          }
+          for (int e = 0; e < 4; ++e) c[q][e] = cn[q][e];
       }
     }
     __syncwarp();
@@ -496,8 +377,6 @@ __global__ void __launch_bounds__(kPanelThreads, 1) panel_kernel(const PanelArgs
     lo = hi;
     hi = hh;
   }
-  if constexpr (MODE != kPanelSddmm)
-    panel_spmm_out<BW, RW>(a, acc, part, slot, warp, lane, nl, first, W0, W1);
 }
 
 template <typename K>
@@ -547,9 +426,13 @@ int64_t panel_min_nnz() {
   return int64_t(1) << 21;
 }
 
-bool panel_fits(const PanelTable &t, int bw) {
-  return t.d_part != nullptr && t.lines_max <= kPanelLinesPerWarp &&
-         (bw == 8 || bw == 16 || bw == 32 || bw == 64) && t.d_off[width_index(bw)] != nullptr;
+bool panel_fits(const PanelTable &t, int bw, double mean_len, int64_t n_op) {
+  if (t.d_part == nullptr || t.lines_max > kPanelLinesPerWarp ||
+      !(bw == 8 || bw == 16 || bw == 32 || bw == 64) || t.d_off[width_index(bw)] == nullptr)
+    return false;
+  // mean entries of a row per panel: the sweep pays only on long runs
+  const double pw = (double)(kStageBytes / (4 * bw));
+  return mean_len * pw / (double)n_op >= 64.0;
 }
 
 namespace {
@@ -603,23 +486,16 @@ void free_panel_table(PanelTable &t) {
   t = PanelTable();
 }
 
-cudaError_t launch_panel(int mode, int bw, const PanelTable &t, const PanelArgs &args, bool pdl,
-                         cudaStream_t s) {
+cudaError_t launch_panel_sddmm(int bw, const PanelTable &t, const PanelArgs &args, bool pdl,
+                               cudaStream_t s) {
   PanelArgs a = args;
   a.part = t.d_part;
   a.off = t.d_off[width_index(bw)];
   a.lines = t.lines;
-  const size_t smem = (size_t)kStages * kStageBytes + (size_t)kConsumers * bw * 4;
-#define SNACK_PANEL(W)                                                                         \
-  case W:                                                                                      \
-    if (mode == kPanelSpmm)                                                                    \
-      return launch_panel_kernel(panel_kernel<W, kPanelLinesPerWarp, kPanelSpmm>, a, t.ctas,   \
-                                 smem, pdl, s);                                                \
-    if (mode == kPanelSpmmPerm)                                                                \
-      return launch_panel_kernel(panel_kernel<W, kPanelLinesPerWarp, kPanelSpmmPerm>, a,       \
-                                 t.ctas, smem, pdl, s);                                        \
-    return launch_panel_kernel(panel_kernel<W, kPanelLinesPerWarp, kPanelSddmm>, a, t.ctas,    \
-                               smem, pdl, s);
+  const size_t smem = (size_t)kStages * kStageBytes;
+#define SNACK_PANEL(W) \
+  case W:              \
+    return launch_panel_kernel(panel_sddmm<W, kPanelLinesPerWarp>, a, t.ctas, smem, pdl, s);
   switch (bw) {
     SNACK_PANEL(8)
     SNACK_PANEL(16)

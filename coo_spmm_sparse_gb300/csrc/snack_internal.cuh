@@ -36,12 +36,11 @@ namespace snack {
 constexpr int kMaxSlice = 256;  // widest batch slice one kernel launch handles
 constexpr int kOptNone = 0, kOptSgd = 1, kOptAdam = 2;  // optimizer kinds
 
-// Entry-balanced partition of a line table for the column-panel kernels
-// (panel.cu): per CTA 32 int4, warps 0-30 {first entry, end entry, first
-// line, lines} and {first line, end line} of the CTA.  Built at topology
-// time for layers of at least panel_min_nnz() entries.
+// Entry-balanced partition of the row table for the column-panel SDDMM
+// (panel.cu): per CTA 32 int4, one per consumer warp {first entry, end
+// entry, first line, lines}, then {first line, end line} of the CTA.  Built
+// at topology time for layers of at least panel_min_nnz() entries.
 constexpr int kPanelLinesPerWarp = 4;  // lines one consumer warp can hold
-constexpr int kPanelSpmm = 0, kPanelSpmmPerm = 1, kPanelSddmm = 2;  // panel kernel modes
 
 constexpr int kPanelWidths = 4;  // slices of 8, 16, 32, 64 floats
 
@@ -147,24 +146,18 @@ struct SddmmArgs {
   OptArgs opt;       // optimizer step fused in instead of writing dw (slices of 1-4)
 };
 
-// Everything a column-panel launch needs (panel.cu).
+// Everything a column-panel SDDMM launch needs (panel.cu).
 struct PanelArgs {
-  const int4 *part;      // the table's partition (set by the launcher)
-  const int32_t *ptr;    // line pointer [lines + 1]
-  const int32_t *idx;    // operand index of each entry, line order
-  const float *val;      // values in line order (canonical, or the column-ordered copy)
-  const int32_t *perm;   // column order -> canonical position (kPanelSpmmPerm)
-  const float *src;      // transposed operand [n_op][bw]
-  int64_t n_op;          // operand lines
-  float *dst;            // SpMM output, element (b, line) at dst[b * ld + line]
-  int64_t ld;
-  int nb;                // valid batch rows of the slice
-  const float *dyt;      // dW: transposed dY [lines][bw]
+  const int4 *part;      // the row table's partition (set by the launcher)
+  const int32_t *idx;    // column of each entry, canonical order
+  const float *src;      // transposed X slice [n_op][bw]
+  int64_t n_op;          // X^T lines (in_features)
+  const float *dyt;      // transposed dY slice [rows][bw]
   float *dw;             // dW output (canonical order)
-  int accumulate;        // dW: add to dw (batch slices after the first)
+  int accumulate;        // add to dw (batch slices after the first)
   int *err;              // the layer's device error flag
   const int32_t *off;    // the table's run offsets for this width (set by the launcher)
-  int64_t lines;         // lines of the table (row stride of off)
+  int64_t lines;         // rows of the table (row stride of off)
 };
 
 // Kernel selection: batch slice width, lanes per entry group, lanes per segment.
@@ -198,10 +191,12 @@ cudaError_t launch_backward_fused(const Plan &pc, const SpmmArgs &cols, const Pl
 bool resident_fits(int bw, int64_t n_op, int64_t nseg, int64_t nnz);
 cudaError_t launch_resident_spmm(bool perm, const Plan &p, const SpmmArgs &a, int64_t n_op,
                                  int *err, bool pdl, cudaStream_t s);
-// Column-panel kernels (slices of 8-64 floats) on a table with a partition.
-bool panel_fits(const PanelTable &t, int bw);
-cudaError_t launch_panel(int mode, int bw, const PanelTable &t, const PanelArgs &a, bool pdl,
-                         cudaStream_t s);
+// Column-panel SDDMM (slices of 8-64 floats) on the row table, when it has a
+// partition and its rows' runs per panel are long (mean_len entries per row,
+// n_op = in_features).
+bool panel_fits(const PanelTable &t, int bw, double mean_len, int64_t n_op);
+cudaError_t launch_panel_sddmm(int bw, const PanelTable &t, const PanelArgs &a, bool pdl,
+                               cudaStream_t s);
 void build_panel_partition(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz, int ctas,
                            std::vector<int4> &part, int *lines_max);
 // Run offsets of every width for a table of `lines` lines over an operand of

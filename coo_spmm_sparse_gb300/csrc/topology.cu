@@ -306,17 +306,24 @@ __global__ void finish_csc(const uint64_t *key, const uint32_t *src, int64_t n, 
 }
 
 // Host: cut lines into segments of at most `cap` entries (balanced parts).
+// Lines up to max(256, 2 x mean) entries stay whole.  On a heavy-tailed
+// table (longest line over 8 x the mean) the cap is instead about the
+// entries one resident team gets on average (nnz / (32 x SMs), kept in
+// [64, 256]): the longest parts otherwise outlast every other team (8192 x
+// 8192 Zipf rows, batch 16: 256-entry parts against ~110 entries per team).
 void build_segments(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz,
                     std::vector<int4> &seg, std::vector<int4> &split, SegTable &t) {
   seg.clear();
   split.clear();
   t.mean_len = nlines > 0 ? (double)nnz / (double)nlines : 0.0;
   t.max_len = 0;
-  const int64_t cap = std::max<int64_t>(256, 2 * (int64_t)std::ceil(t.mean_len));
+  for (int64_t l = 0; l < nlines; ++l) t.max_len = std::max<int64_t>(t.max_len, ptr[l + 1] - ptr[l]);
+  int64_t cap = std::max<int64_t>(256, 2 * (int64_t)std::ceil(t.mean_len));
+  if ((double)t.max_len > 8.0 * t.mean_len)
+    cap = std::min<int64_t>(256, std::max<int64_t>(64, nnz / (32 * (int64_t)device_sms())));
   int64_t slots = 0;
   for (int64_t l = 0; l < nlines; ++l) {
     const int64_t b = ptr[l], e = ptr[l + 1], len = e - b;
-    t.max_len = std::max(t.max_len, len);
     const int64_t parts = len > cap ? (len + cap - 1) / cap : 1;
     if (parts == 1) {
       seg.push_back(make_int4((int)l, (int)b, (int)e, -1));
@@ -399,28 +406,27 @@ snack_status finish_layout(Layer &L, const uint64_t *d_cell_key, cudaStream_t s,
   build_segments(cp, L.in, n, seg, split, L.csc);
   st = upload_segments(seg, split, L.csc, &L.device_bytes, s, err);
   if (st != SNACK_OK) return st;
-  // Column-panel partitions of both tables (large layers only).
-  for (int dir = 0; dir < 2; ++dir) {
-    PanelTable &pt = dir == 0 ? L.csr.panel : L.csc.panel;
+  // Column-panel partition of the row table (large layers only; the panel
+  // SDDMM runs over rows).
+  {
+    PanelTable &pt = L.csr.panel;
     free_panel_table(pt);
-    if (n < panel_min_nnz() || n == 0) continue;
     std::vector<int4> part;
     int lines_max = 0;
     const int ctas = device_sms();
-    const int64_t lines = dir == 0 ? L.out : L.in;
-    build_panel_partition(dir == 0 ? rp : cp, lines, n, ctas, part, &lines_max);
-    if (lines_max > kPanelLinesPerWarp) continue;  // too many lines per warp: no panels
-    TRY_CUDA(dev_alloc(&pt.d_part, part.size(), &L.device_bytes));
-    TRY_CUDA(cudaMemcpyAsync(pt.d_part, part.data(), part.size() * sizeof(int4),
-                             cudaMemcpyHostToDevice, s));
-    TRY_CUDA(build_panel_offsets(pt, dir == 0 ? L.d_row_ptr : L.d_col_ptr,
-                                 dir == 0 ? L.d_col : L.d_csc_row, lines, dir == 0 ? L.in : L.out,
-                                 &L.device_bytes, s));
-    TRY_CUDA(cudaStreamSynchronize(s));
-    pt.ctas = ctas;
-    pt.lines = lines;
-    pt.lines_max = lines_max;
-    pt.bytes += part.size() * sizeof(int4);
+    if (n >= panel_min_nnz() && n > 0)
+      build_panel_partition(rp, L.out, n, ctas, part, &lines_max);
+    if (!part.empty() && lines_max <= kPanelLinesPerWarp) {
+      TRY_CUDA(dev_alloc(&pt.d_part, part.size(), &L.device_bytes));
+      TRY_CUDA(cudaMemcpyAsync(pt.d_part, part.data(), part.size() * sizeof(int4),
+                               cudaMemcpyHostToDevice, s));
+      TRY_CUDA(build_panel_offsets(pt, L.d_row_ptr, L.d_col, L.out, L.in, &L.device_bytes, s));
+      TRY_CUDA(cudaStreamSynchronize(s));
+      pt.ctas = ctas;
+      pt.lines = L.out;
+      pt.lines_max = lines_max;
+      pt.bytes += part.size() * sizeof(int4);
+    }
   }
   // Split workspace: partial slots and re-armed tickets (zero between calls).
   if (L.d_partial) cudaFree(L.d_partial);
