@@ -309,8 +309,10 @@ __global__ void finish_csc(const uint64_t *key, const uint32_t *src, int64_t n, 
 // Lines up to max(256, 2 x mean) entries stay whole.  On a heavy-tailed
 // table (longest line over 8 x the mean) the cap is instead about the
 // entries one resident team gets on average (nnz / (32 x SMs), kept in
-// [64, 256]): the longest parts otherwise outlast every other team (8192 x
-// 8192 Zipf rows, batch 16: 256-entry parts against ~110 entries per team).
+// [64, 256]): the longest parts otherwise outlast the other teams (8192 x
+// 8192 Zipf rows, batch 16: 23.0 us with 256-entry parts, 21.8 us with 138;
+// 64-entry parts measured 29.4 us, their combines and a second wave of
+// teams costing more than the balance gained).
 void build_segments(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz,
                     std::vector<int4> &seg, std::vector<int4> &split, SegTable &t) {
   seg.clear();
