@@ -35,7 +35,7 @@
  *     the handle as it was.
  *   - Limits: 1 <= out_features, in_features < 2^31; 0 <= nnz < 2^31 and
  *     nnz <= out_features * in_features; batch >= 1 (any size: batches above
- *     256 run as consecutive slices of 256).
+ *     256 run as consecutive slices of 256, each padded to a power of two).
  */
 #ifndef SNACK_H
 #define SNACK_H
@@ -243,7 +243,9 @@ snack_status snack_export_segments(snack_handle h, int32_t *row_ptr, int32_t *co
 /*
  * Which kernel variant a call would run: for op 0 = forward, 1 =
  * backward_input, 2 = backward_weight and the given batch, returns the
- * batch slice width (1, 2, 4, 8, 16, 32, 64, 128 or 256), the lanes that
+ * width of its first batch slice (1, 2, 4, 8, 16, 32, 64, 128 or 256; on
+ * layers of 2^21+ entries a batch just above a power of two w >= 32 runs as
+ * a slice of w and one of the remainder), the lanes that
  * share one row (or column) segment (the launch may halve them when that
  * keeps every segment in one wave of resident teams), the number of
  * segments, and where the dense operand is gathered from: 0 = global memory

@@ -143,7 +143,9 @@ def _sampled_large(sparsity, batches):
 
 @pytest.mark.parametrize("sparsity", [99, 95, 90])
 def test_large_layer_full_size_sampled(sparsity):
-    _sampled_large(sparsity, [1, 4, 8, 16, 64])
+    # 33 and 65 on the 95 % layer: batches just above a power of two, cut into
+    # a power-of-two slice and a small remainder on large layers
+    _sampled_large(sparsity, [1, 4, 8, 16, 64] + ([33, 65] if sparsity == 95 else []))
 
 
 def test_large99_full_oracle_b16():
@@ -377,6 +379,14 @@ def test_plan_follows_batch_and_row_length():
     assert sn().snack_plan(h5, 1, 2, with_resident=True)[3] == 1
     assert sn().snack_plan(h5, 0, 4, with_resident=True)[3] == 0
     assert sn().snack_plan(h5, 0, 16, with_resident=True)[3] == 0
+    # dW of the 5 M-entry layer sweeps its operand in column panels while a
+    # row's run per panel is long (500 entries per row: batch 8, not 16)
+    assert sn().snack_plan(h5, 2, 8, with_resident=True)[3] == 2
+    assert sn().snack_plan(h5, 2, 16, with_resident=True)[3] == 0
+    # on a large layer a batch just above a power of two w >= 32 starts
+    # with a slice of w (the remainder follows as its own slice)
+    for B, w in ((9, 16), (33, 32), (40, 32), (41, 64), (65, 64), (129, 128), (300, 256)):
+        assert sn().snack_plan(h5, 0, B)[0] == w, B
     small = workloads.workload("toy256").layers[0]
     r, c, v = small.coo()
     h2 = sn().snack_create(small.out, small.inp, r, c, v)
