@@ -311,8 +311,11 @@ __global__ void finish_csc(const uint64_t *key, const uint32_t *src, int64_t n, 
 // entries one resident team gets on average (nnz / (32 x SMs), kept in
 // [64, 256]): the longest parts otherwise outlast the other teams (8192 x
 // 8192 Zipf rows, batch 16: 23.0 us with 256-entry parts, 21.8 us with 138;
-// 64-entry parts measured 29.4 us, their combines and a second wave of
-// teams costing more than the balance gained).
+// parts of 64 / 96 / 112 / 192 entries measured 29.8 / 27.0 / 24.0 / 22.1
+// us, the combines and a second wave of teams of the shorter parts costing
+// more than the balance gained.  Emitting the segments longest line first
+// and dealing them to the teams in snake order across rounds measured
+// 22.6-25.0 us at those part sizes and was not kept).
 void build_segments(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz,
                     std::vector<int4> &seg, std::vector<int4> &split, SegTable &t) {
   seg.clear();
