@@ -268,6 +268,49 @@ def test_long_rows_and_columns_split():
     assert segs > out
 
 
+def _heavy_tailed(out, inp, full_rows, seed):
+    """Rows of 0-30 entries (geometric, a tenth of them empty) plus a few full
+    rows: a heavy-tailed table, its long rows cut into many parts."""
+    g = np.random.default_rng(seed)
+    lens = np.minimum(g.geometric(0.09, out) - 1, 30)
+    lens[g.random(out) < 0.1] = 0
+    lens[full_rows] = inp
+    cells = np.concatenate([r * inp + g.choice(inp, n, replace=False)
+                            for r, n in enumerate(lens) if n > 0])
+    g.shuffle(cells)
+    row = (cells // inp).astype(np.int32)
+    col = (cells % inp).astype(np.int32)
+    val = g.standard_normal(cells.size).astype(np.float32)
+    return row, col, val
+
+
+def test_heavy_tailed_rows_with_empty_rows():
+    out, inp = 3000, 2000
+    row, col, val = _heavy_tailed(out, inp, [5, 1234, 2999, 3000 // 2], seed=11)
+    # every slice width (1-256), odd batches, and the slice split above 256
+    h, ref = _layer_case(out, inp, row, col, val, [1, 2, 3, 5, 8, 16, 17, 33, 64, 100, 256, 300],
+                         seed=12)
+    _, _, segs = sn().snack_plan(h, 0, 16)
+    assert segs > out  # the full rows are split
+    # split-row tickets re-arm: identical bits on a second call
+    X = to_dev(np.random.default_rng(13).standard_normal((16, inp)).astype(np.float32))
+    Y1 = sn().snack_forward(h, X)
+    Y2 = sn().snack_forward(h, X)
+    torch.cuda.synchronize()
+    assert torch.equal(Y1, Y2)
+    # the segment tables are rebuilt with the topology
+    pruned, trials = sn().snack_prune_regrow(h, 0.3, 21)
+    o = oracle.prune_regrow(out, inp, ref["row"], ref["col"], ref["val"], 0.3, 21)
+    assert (pruned, trials) == (o["pruned"], o["trials"])
+    ref2 = canonical(out, inp, o["row"], o["col"], o["val"])
+    check_topology(h, ref2)
+    g = np.random.default_rng(14)
+    for B in (1, 16, 64):
+        Xb = g.standard_normal((B, inp)).astype(np.float32)
+        dY = g.standard_normal((B, out)).astype(np.float32)
+        check_products(h, out, inp, ref2, Xb, dY, fused=False)
+
+
 def test_identity_pattern_bit_exact():
     n = 4099
     idx = np.arange(n, dtype=np.int32)
