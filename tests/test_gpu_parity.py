@@ -311,6 +311,25 @@ def test_heavy_tailed_rows_with_empty_rows():
         check_products(h, out, inp, ref2, Xb, dY, fused=False)
 
 
+def test_halved_lines_wide_slices():
+    # 2.2 M entries over 4096 x 4096 (537 per row and column): 64-wide
+    # slices walk every line in two halves, combined by the split-line path;
+    # every product, the fused backward included, against the oracle
+    out = inp = 4096
+    h0, _ = sn().snack_create_random(out, inp, 2_200_000, 31)
+    row, col, _ = sn().snack_export(h0)
+    val = np.random.default_rng(32).standard_normal(row.size).astype(np.float32)
+    h, ref = _layer_case(out, inp, row, col, val, [64, 41, 100, 16], seed=33)
+    assert sn().snack_plan(h, 0, 64)[2] == 2 * out
+    assert sn().snack_plan(h, 1, 64)[2] == 2 * inp
+    # the halves' tickets re-arm: identical bits on a second call
+    X = to_dev(np.random.default_rng(34).standard_normal((64, inp)).astype(np.float32))
+    Y1 = sn().snack_forward(h, X)
+    Y2 = sn().snack_forward(h, X)
+    torch.cuda.synchronize()
+    assert torch.equal(Y1, Y2)
+
+
 def test_identity_pattern_bit_exact():
     n = 4099
     idx = np.arange(n, dtype=np.int32)
@@ -430,6 +449,13 @@ def test_plan_follows_batch_and_row_length():
     # with a slice of w (the remainder follows as its own slice)
     for B, w in ((9, 16), (33, 32), (40, 32), (41, 64), (65, 64), (129, 128), (300, 256)):
         assert sn().snack_plan(h5, 0, B)[0] == w, B
+    # 64-wide slices of a large layer of long lines walk its lines in halves
+    # (two segments per row or column); other widths and small layers do not
+    for op in (0, 1, 2):
+        assert sn().snack_plan(h5, op, 64)[2] == 2 * L.out
+        assert sn().snack_plan(h5, op, 32)[2] == L.out
+        assert sn().snack_plan(h5, op, 128)[2] == L.out
+    assert sn().snack_plan(h, 0, 64)[2] == L.out
     small = workloads.workload("toy256").layers[0]
     r, c, v = small.coo()
     h2 = sn().snack_create(small.out, small.inp, r, c, v)
