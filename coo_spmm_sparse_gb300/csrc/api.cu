@@ -169,12 +169,29 @@ int sddmm_subranges(const snack::SegTable &t, const snack::Plan &p) {
   return nsub;
 }
 
+// Whether the split lines of an SpMM over table t with plan q are summed by
+// a second pass (split_sums) instead of by the last part's team: for slices
+// of 16+ floats, where the tickets' fences and the serial sum of the parts
+// sit on the kernel's critical path (10000 x 10000 at 95 %, halved lines,
+// batch 64 forward 91.1 -> 84.7 us; 8192 x 8192 Zipf rows, batch 16 20.8 ->
+// 20.1).  At narrower slices the extra launch costs what it saves (Zipf
+// rows, batch 1: 12.2 -> 12.4 us).
+bool two_pass(const snack::SegTable &t, const snack::Plan &q) {
+  return t.nsplit > 0 && q.bw >= 16;
+}
+
 // dX over the column segments: through the permutation, or (values in
 // column order) with the canonical-order kernels.
 cudaError_t launch_cols(const snack::SegTable &t, const snack::Plan &p, snack::SpmmArgs a, int nb,
                         cudaStream_t s) {
   const snack::Plan q = sub_slices(t, p, nb, &a.nsub);
-  return a.perm ? snack::launch_spmm_cols(q, a, true, s) : snack::launch_spmm_rows(q, a, true, s);
+  const bool two = two_pass(t, q);
+  if (two) a.counter = nullptr;
+  cudaError_t e =
+      a.perm ? snack::launch_spmm_cols(q, a, true, s) : snack::launch_spmm_rows(q, a, true, s);
+  if (e != cudaSuccess || !two) return e;
+  g_launches.fetch_add(1, std::memory_order_relaxed);  // the first; the caller counts the second
+  return snack::launch_split_sums(q.bw, a, t.nsplit, true, s);
 }
 
 // Rows of the next batch slice when `left` rows remain: at most kMaxSlice.
@@ -222,7 +239,13 @@ snack_status run_forward(snack_handle h, const float *X, float *Y, int64_t batch
       e = snack::launch_resident_spmm(false, p, a, L.in, L.d_err, true, s);
     } else {
       const snack::Plan q = sub_slices(t, p, nb, &a.nsub);
+      const bool two = two_pass(t, q);
+      if (two) a.counter = nullptr;
       e = snack::launch_spmm_rows(q, a, true, s);
+      if (e == cudaSuccess && two) {
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        e = snack::launch_split_sums(q.bw, a, t.nsplit, true, s);
+      }
     }
     if (e != cudaSuccess) return cuda_fail(h, e, "forward launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);

@@ -187,6 +187,10 @@ int entry_lanes(int bw);
 // stream (the kernels wait for it before touching any memory it may use).
 cudaError_t launch_spmm_rows(const Plan &p, const SpmmArgs &a, bool pdl, cudaStream_t s);
 cudaError_t launch_spmm_cols(const Plan &p, const SpmmArgs &a, bool pdl, cudaStream_t s);
+// Second pass summing the split lines' partials of an SpMM launched with
+// a.counter null (bw = that launch's slice width).
+cudaError_t launch_split_sums(int bw, const SpmmArgs &a, int64_t nsplit, bool pdl,
+                              cudaStream_t s);
 cudaError_t launch_sddmm(const Plan &p, const SddmmArgs &a, bool pdl, cudaStream_t s);
 // The same with the optimizer step of a.opt applied instead of writing dW.
 cudaError_t launch_sddmm_step(const Plan &p, const SddmmArgs &a, bool pdl, cudaStream_t s);

@@ -443,6 +443,7 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
 #pragma unroll
         for (int i = 0; i < VEC; ++i) mine[v * G * VEC + i] = acc[v][i];
     }
+    if (a.counter == nullptr) continue;  // the parts are summed by split_sums
     __threadfence();
     const unsigned tmask = lps == 32 ? 0xffffffffu : (((1u << lps) - 1u) << (lane - tlane));
     __syncwarp(tmask);
@@ -711,6 +712,34 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, 
 #pragma unroll
         for (int e = 0; e < 4; ++e) c[q][e] = cn[q][e];
     }
+  }
+}
+
+// Second pass of an SpMM whose split lines only parked their parts'
+// partials (launched with a.counter null): warp w sums split line w's parts
+// in part order and writes the line's outputs.  Its grid-dependency wait
+// makes the first pass's partials visible.
+template <int BW>
+__global__ void __launch_bounds__(256) split_sums(const SpmmArgs a, int64_t nsplit) {
+  griddep_wait();
+  const int64_t w = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
+  if (w >= nsplit) return;
+  const int lane = threadIdx.x & 31;
+  const int4 sp = a.split[w];
+  const int line = a.seg[sp.x].x;
+  for (int b = lane; b < BW && b < a.nb; b += 32) {
+    const float *q = a.partial + (int64_t)sp.z * BW + b;
+    float t = 0.f;
+    int p = 0;
+    for (; p + 8 <= sp.y; p += 8) {
+      float x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] = __ldcg(q + (int64_t)(p + u) * BW);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) t += x[u];
+    }
+    for (; p < sp.y; ++p) t += __ldcg(q + (int64_t)p * BW);
+    a.dst[(int64_t)b * a.ld + line] = t;
   }
 }
 

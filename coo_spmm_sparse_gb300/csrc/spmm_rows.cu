@@ -14,4 +14,22 @@ cudaError_t launch_spmm_rows(const Plan &p, const SpmmArgs &args, bool pdl, cuda
 #undef SNACK_CALL
 }
 
+cudaError_t launch_split_sums(int bw, const SpmmArgs &a, int64_t nsplit, bool pdl,
+                              cudaStream_t s) {
+  if (nsplit == 0) return cudaSuccess;
+  const int64_t blocks = (nsplit * 32 + 255) / 256;
+  switch (bw) {
+    case 1: return launch_ex(split_sums<1>, blocks, pdl, s, a, nsplit);
+    case 2: return launch_ex(split_sums<2>, blocks, pdl, s, a, nsplit);
+    case 4: return launch_ex(split_sums<4>, blocks, pdl, s, a, nsplit);
+    case 8: return launch_ex(split_sums<8>, blocks, pdl, s, a, nsplit);
+    case 16: return launch_ex(split_sums<16>, blocks, pdl, s, a, nsplit);
+    case 32: return launch_ex(split_sums<32>, blocks, pdl, s, a, nsplit);
+    case 64: return launch_ex(split_sums<64>, blocks, pdl, s, a, nsplit);
+    case 128: return launch_ex(split_sums<128>, blocks, pdl, s, a, nsplit);
+    case 256: return launch_ex(split_sums<256>, blocks, pdl, s, a, nsplit);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace snack
