@@ -44,7 +44,8 @@ constexpr int kPanelLinesPerWarp = 4;  // lines one consumer warp can hold
 
 constexpr int kPanelWidths = 4;  // slices of 8, 16, 32, 64 floats
 
-// Slice width that walks the halved-line tables (Layer::csr_half): at 64
+// Widest slice that walks the halved-line tables (Layer::csr_half): the
+// SpMMs at exactly this width, the SDDMM from 32 floats up to it.  At 64
 // floats per entry a team's walk of a long line is latency-bound, and the
 // last round of teams runs mostly empty.
 constexpr int kHalfLineWidth = 64;

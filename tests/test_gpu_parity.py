@@ -313,13 +313,14 @@ def test_heavy_tailed_rows_with_empty_rows():
 
 def test_halved_lines_wide_slices():
     # 2.2 M entries over 4096 x 4096 (537 per row and column): 64-wide
-    # slices walk every line in two halves, combined by the split-line path;
-    # every product, the fused backward included, against the oracle
+    # slices walk every line in two halves, combined by the split-line path
+    # (the weight product from 32-wide slices on); every product, the fused
+    # backward included, against the oracle
     out = inp = 4096
     h0, _ = sn().snack_create_random(out, inp, 2_200_000, 31)
     row, col, _ = sn().snack_export(h0)
     val = np.random.default_rng(32).standard_normal(row.size).astype(np.float32)
-    h, ref = _layer_case(out, inp, row, col, val, [64, 41, 100, 16], seed=33)
+    h, ref = _layer_case(out, inp, row, col, val, [64, 41, 100, 32, 16], seed=33)
     assert sn().snack_plan(h, 0, 64)[2] == 2 * out
     assert sn().snack_plan(h, 1, 64)[2] == 2 * inp
     # the halves' tickets re-arm: identical bits on a second call
@@ -453,7 +454,8 @@ def test_plan_follows_batch_and_row_length():
     # (two segments per row or column); other widths and small layers do not
     for op in (0, 1, 2):
         assert sn().snack_plan(h5, op, 64)[2] == 2 * L.out
-        assert sn().snack_plan(h5, op, 32)[2] == L.out
+        assert sn().snack_plan(h5, op, 32)[2] == (2 * L.out if op == 2 else L.out)
+        assert sn().snack_plan(h5, op, 16)[2] == L.out
         assert sn().snack_plan(h5, op, 128)[2] == L.out
     assert sn().snack_plan(h, 0, 64)[2] == L.out
     small = workloads.workload("toy256").layers[0]
