@@ -97,16 +97,15 @@ snack_status finish_create(snack_layer *h, snack_status st, const std::string &e
 }
 
 // The row (rows) or column table a slice of nb batch rows walks: the halved
-// lines where built, unless `halves` is off, for SpMM slices of
-// kHalfLineWidth and SDDMM slices of 32 to kHalfLineWidth (its entries need
-// no combining: 10000 x 10000, batch 32, dW at 90 % 123.9 -> 106.1 us, at
-// 95 % 66.3 -> 59.9; the SpMMs lost there, 101.8 -> 106.7 and 58.5 -> 59.3).
-const snack::SegTable &line_table(const snack::Layer &L, bool rows, int64_t nb, bool sddmm,
-                                  bool halves = true) {
+// lines where built, for SpMM slices of kHalfLineWidth and SDDMM slices of
+// 32 to kHalfLineWidth (its entries need no combining: 10000 x 10000, batch
+// 32, dW at 90 % 123.9 -> 106.1 us, at 95 % 66.3 -> 59.9; the SpMMs lost
+// there, 101.8 -> 106.7 and 58.5 -> 59.3).
+const snack::SegTable &line_table(const snack::Layer &L, bool rows, int64_t nb, bool sddmm) {
   const snack::SegTable &half = rows ? L.csr_half : L.csc_half;
   const int w = snack::slice_width(std::min<int64_t>(nb, snack::kMaxSlice));
   const bool wide = sddmm ? (w >= 32 && w <= snack::kHalfLineWidth) : w == snack::kHalfLineWidth;
-  if (halves && half.nseg > 0 && wide) return half;
+  if (half.nseg > 0 && wide) return half;
   return rows ? L.csr : L.csc;
 }
 
@@ -266,12 +265,14 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
                                 const snack::OptArgs *opt = nullptr) {
   snack::Layer &L = h->L;
   const bool fused_opt = opt && opt->kind != snack::kOptNone;
-  // Both products at once keep the whole lines: the shared-grid kernel gains
-  // little from halved ones (10000 x 10000, batch 64: at 90 % 312 -> 306 us,
-  // at 95 % 158 -> 172).
-  const bool halves = !(dX && dW);
-  const snack::SegTable &tc = line_table(L, false, nb, false, halves);
-  const snack::SegTable &tr = line_table(L, true, nb, true, halves);
+  // Both products in the shared-grid kernel walk halved lines only where
+  // both of them do (64-wide slices), its grid being split by segment
+  // counts: 10000 x 10000, batch 64, 90 % 307.6 -> 285.7 us, 95 % 157.8 ->
+  // 154.1 (dX's halves summed by the second pass); halving only the rows at
+  // 32-wide slices measured 194.6 -> 227.8.
+  const bool both = dX && dW;
+  const snack::SegTable &tc = line_table(L, false, nb, false);
+  const snack::SegTable &tr = line_table(L, true, nb, !both);
   const snack::Plan pc = snack::choose_plan(tc, nb);
   const snack::Plan pr = snack::choose_plan(tr, nb);
   if (fused_opt && dX) return fail(h, SNACK_ERR_INVALID_ARG, "an optimizer step reads no dX");
@@ -363,9 +364,15 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     }
     return SNACK_OK;
   }
-  if (dX && want_w)
+  if (dX && want_w) {
+    const bool two = two_pass(tc, pc);
+    if (two) cols.counter = nullptr;
     e = snack::launch_backward_fused(pc, cols, pr, rows, true, s);
-  else if (dX)
+    if (e == cudaSuccess && two) {
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+      e = snack::launch_split_sums(pc.bw, cols, tc.nsplit, true, s);
+    }
+  } else if (dX)
     e = launch_cols(tc, pc, cols, nb, s);
   else
     e = snack::launch_sddmm(pr, rows, true, s);
