@@ -265,14 +265,19 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
                                 const snack::OptArgs *opt = nullptr) {
   snack::Layer &L = h->L;
   const bool fused_opt = opt && opt->kind != snack::kOptNone;
-  // Both products in the shared-grid kernel walk halved lines only where
-  // both of them do (64-wide slices), its grid being split by segment
-  // counts: 10000 x 10000, batch 64, 90 % 307.6 -> 285.7 us, 95 % 157.8 ->
-  // 154.1 (dX's halves summed by the second pass); halving only the rows at
-  // 32-wide slices measured 194.6 -> 227.8.
+  // Both products in the shared-grid kernel (its grid split by segment
+  // counts) walk halved lines on both sides or on neither: from 32-wide
+  // slices on, dX's halves summed by the second pass.  10000 x 10000, batch
+  // 64: 90 % 307.6 -> 285.7 us, 95 % 157.8 -> 154.1; batch 32: 90 % 194.6 ->
+  // 181.9, 95 % 102.5 -> 102.9; batch 16 lost (90 % 116.8 -> 126.7), and so
+  // did halving only the rows at batch 32 (194.6 -> 227.8).
   const bool both = dX && dW;
-  const snack::SegTable &tc = line_table(L, false, nb, false);
-  const snack::SegTable &tr = line_table(L, true, nb, !both);
+  const int w = snack::slice_width(std::min<int64_t>(nb, snack::kMaxSlice));
+  const bool fused_halves = both && w >= 32 && w <= snack::kHalfLineWidth &&
+                            L.csr_half.nseg > 0 && L.csc_half.nseg > 0 &&
+                            !snack::panel_fits(L.csr.panel, w, L.csr.mean_len, L.in);
+  const snack::SegTable &tc = fused_halves ? L.csc_half : line_table(L, false, nb, false);
+  const snack::SegTable &tr = fused_halves ? L.csr_half : line_table(L, true, nb, !both);
   const snack::Plan pc = snack::choose_plan(tc, nb);
   const snack::Plan pr = snack::choose_plan(tr, nb);
   if (fused_opt && dX) return fail(h, SNACK_ERR_INVALID_ARG, "an optimizer step reads no dX");
