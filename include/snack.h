@@ -248,7 +248,10 @@ snack_status snack_export_segments(snack_handle h, int32_t *row_ptr, int32_t *co
  * a slice of w and one of the remainder), the lanes that
  * share one row (or column) segment (the launch may halve them when that
  * keeps every segment in one wave of resident teams), the number of
- * segments, and where the dense operand is gathered from: 0 = global memory
+ * segments (on layers of 2^21+ entries whose lines average 400+ entries,
+ * 64-wide slices of op 0 and 1 and 32- to 64-wide slices of op 2 walk every
+ * line in two halves, so twice the lines), and where the dense operand is
+ * gathered from: 0 = global memory
  * (through L1), 1 = a copy of the whole operand in every block's shared
  * memory, 2 = shared memory one column panel at a time (the column-panel
  * kernels of slices of 8-64 floats on layers with a panel partition).  Any
