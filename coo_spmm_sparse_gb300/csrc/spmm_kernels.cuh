@@ -694,11 +694,12 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, 
     // The column loads run one step ahead of the gathers (as in
     // walk_pipelined).  Two quads per step; one with the optimizer step (its
     // operands take the registers of the second quad), and one for rows of
-    // 128+ floats (64+ inside the fused backward), where the second quad's
-    // gathered rows cost resident warps: 96 -> 64 registers, 2 -> 4 blocks
-    // per SM (10000x10000 @95% batch 256 dW 353 -> 343 us, the decoder
-    // workload's fused backward step +7 %; a standalone 64-wide dW lost 5 %).
-    constexpr int QPS = (OPT || BW >= 128 || (FUSED && BW >= 64)) ? 1 : 2;
+    // 64+ floats, where the second quad's gathered rows cost resident warps:
+    // 96 -> 64 registers, 2 -> 4 blocks per SM (10000x10000 @95% batch 256 dW
+    // 353 -> 343 us, the decoder workload's fused backward step +7 %; batch
+    // 64 dW over halved rows at 95 % 93.2 -> 87.3 us, at 99 % 33.5 -> 31.1,
+    // at 90 % 167.9 -> 168.1).
+    constexpr int QPS = (OPT || BW >= 64) ? 1 : 2;
     int kb = (k0 & ~3) + 4 * grp;
     int c[2][4] = {};
     load_col_step<QPS>(a.col, kb, k1, npt, c);
