@@ -373,12 +373,12 @@ void build_halves(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz,
   t.nslots = slots;
 }
 
-// Whether a table of `nlines` lines gets its halved copy: a large layer
-// (2^21+ entries) of long, evenly filled lines.  Measured on 10000 x 10000
-// at 90 % (1000 entries per line), 64-wide slices: forward 182 -> 159 us,
-// dX 180 -> 157, dW 187 -> 166; at narrower slices the halves' combines
-// cost more than they save (batch 8 forward 44 -> 63 us), so only
-// kHalfLineWidth slices walk them.
+// Whether table t gets its halved copy: a large layer (2^21+ entries) of
+// long, evenly filled lines.  Measured on 10000 x 10000 at 90 % (1000
+// entries per line), 64-wide slices: forward 182 -> 159 us, dX 180 -> 157,
+// dW 187 -> 166.  Which slices walk the halves is decided per product at
+// launch (the SpMMs' combines cost more than they save on narrow slices:
+// batch 8 forward 44 -> 63 us).
 bool halves_pay(const SegTable &t, int64_t nnz) {
   return nnz >= (int64_t(1) << 21) && t.mean_len >= 400.0 && (double)t.max_len <= 8.0 * t.mean_len;
 }
