@@ -70,12 +70,15 @@ void account(snack::Layer &L) {
   size_t b = 0;
   b += (size_t)L.nnz_pad * 4 * 5;  // col, row, val, csc_row, csc_perm
   b += (size_t)(L.out + 1 + L.in + 1) * 4;
-  for (const snack::SegTable *t : {&L.csr, &L.csc, &L.csr_half, &L.csc_half})
+  for (const snack::SegTable *t :
+       {&L.csr, &L.csc, &L.csr_half, &L.csc_half, &L.csr_third, &L.csc_third})
     b += (size_t)(t->nseg + t->nsplit) * sizeof(int4);
   b += L.csr.panel.bytes + L.csc.panel.bytes;
   b += (size_t)(L.in + L.out) * snack::kMaxSlice * 4;
   b += snack::partial_floats(L) * 4;
-  b += (size_t)std::max({L.csr.nsplit, L.csc.nsplit, L.csr_half.nsplit, L.csc_half.nsplit}) * 4;
+  b += (size_t)std::max({L.csr.nsplit, L.csc.nsplit, L.csr_half.nsplit, L.csc_half.nsplit,
+                         L.csr_third.nsplit, L.csc_third.nsplit}) *
+       4;
   b += 4;  // error flag
   // column-ordered values; optimizer state, gradient buffer
   const void *extra[] = {L.d_val_csc, L.d_opt[0], L.d_opt[1], L.d_gacc};
@@ -96,16 +99,20 @@ snack_status finish_create(snack_layer *h, snack_status st, const std::string &e
   return SNACK_OK;
 }
 
-// The row (rows) or column table a slice of nb batch rows walks: the halved
-// lines where built, for SpMM slices of kHalfLineWidth and SDDMM slices of
-// 32 to kHalfLineWidth (its entries need no combining: 10000 x 10000, batch
-// 32, dW at 90 % 123.9 -> 106.1 us, at 95 % 66.3 -> 59.9; the SpMMs lost
-// there, 101.8 -> 106.7 and 58.5 -> 59.3).
+// The row (rows) or column table one product (SpMM or SDDMM) walks for a
+// slice of nb batch rows, where the cut copies are built: slices of
+// kHalfLineWidth walk the lines in thirds (10000 x 10000 at 90 %, batch 64:
+// forward / dX / dW 157 / 156 / 169 us with halves, 148 / 149 / 157 with
+// thirds; at 95 % dW 88 -> 84), 32-wide slices of the SDDMM in halves (its
+// entries need no combining: batch 32 dW at 90 % 123.9 -> 106.1 us, at 95 %
+// 66.3 -> 59.9; thirds 106.6 / 61.7, and the SpMMs lost there, 101.8 ->
+// 106.7 and 58.5 -> 59.3 with halves).
 const snack::SegTable &line_table(const snack::Layer &L, bool rows, int64_t nb, bool sddmm) {
   const snack::SegTable &half = rows ? L.csr_half : L.csc_half;
+  const snack::SegTable &third = rows ? L.csr_third : L.csc_third;
   const int w = snack::slice_width(std::min<int64_t>(nb, snack::kMaxSlice));
-  const bool wide = sddmm ? (w >= 32 && w <= snack::kHalfLineWidth) : w == snack::kHalfLineWidth;
-  if (half.nseg > 0 && wide) return half;
+  if (w == snack::kHalfLineWidth && third.nseg > 0) return third;
+  if (sddmm && w == 32 && half.nseg > 0) return half;
   return rows ? L.csr : L.csc;
 }
 
@@ -270,7 +277,8 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
   // slices on, dX's halves summed by the second pass.  10000 x 10000, batch
   // 64: 90 % 307.6 -> 285.7 us, 95 % 157.8 -> 154.1; batch 32: 90 % 194.6 ->
   // 181.9, 95 % 102.5 -> 102.9; batch 16 lost (90 % 116.8 -> 126.7), and so
-  // did halving only the rows at batch 32 (194.6 -> 227.8).
+  // did halving only the rows at batch 32 (194.6 -> 227.8); thirds measured
+  // the same at batch 64 and slower at 32 (95 %: 101.4 -> 107.0).
   const bool both = dX && dW;
   const int w = snack::slice_width(std::min<int64_t>(nb, snack::kMaxSlice));
   const bool fused_halves = both && w >= 32 && w <= snack::kHalfLineWidth &&

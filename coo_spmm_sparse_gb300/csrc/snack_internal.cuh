@@ -44,10 +44,9 @@ constexpr int kPanelLinesPerWarp = 4;  // lines one consumer warp can hold
 
 constexpr int kPanelWidths = 4;  // slices of 8, 16, 32, 64 floats
 
-// Widest slice that walks the halved-line tables (Layer::csr_half): the
-// SpMMs at exactly this width, the SDDMM from 32 floats up to it.  At 64
-// floats per entry a team's walk of a long line is latency-bound, and the
-// last round of teams runs mostly empty.
+// Widest slice that walks the cut-line tables (Layer::csr_half, csr_third):
+// at 64 floats per entry a team's walk of a long line is latency-bound, and
+// the last round of teams runs mostly empty.
 constexpr int kHalfLineWidth = 64;
 
 struct PanelTable {
@@ -88,10 +87,10 @@ struct Layer {
   bool values_shared = false;      // a writable values pointer is out (snack_values)
   int32_t *d_col_ptr = nullptr;
   SegTable csr, csc;
-  // The same lines cut into two balanced parts each, for slices of
-  // kHalfLineWidth on layers of 2^21+ entries whose lines average 400+
-  // entries (nseg 0 when not built).
-  SegTable csr_half, csc_half;
+  // The same lines cut into two (and three) balanced parts each, for wide
+  // slices on layers of 2^21+ entries whose lines average 400+ entries
+  // (nseg 0 when not built).
+  SegTable csr_half, csc_half, csr_third, csc_third;
   // workspace
   float *d_xt = nullptr;       // [in][kMaxSlice]   transposed X slice
   float *d_dyt = nullptr;      // [out][kMaxSlice]  transposed dY slice
@@ -248,7 +247,7 @@ snack_status prune_regrow(Layer &L, float frac, uint64_t seed, int64_t *pruned,
                           int64_t *trials, cudaStream_t s, std::string &err);
 void free_layer(Layer &L);
 // Floats of the split-line partial workspace: kMaxSlice per slot of the
-// row and column tables, kHalfLineWidth per slot of the halved ones.
+// row and column tables, kHalfLineWidth per slot of their cut copies.
 size_t partial_floats(const Layer &L);
 // val_csc[s] = val[csc_perm[s]]; the copy is current unless a writable
 // values pointer is out.

@@ -346,10 +346,10 @@ void build_segments(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz
   t.nslots = slots;
 }
 
-// Host: every line of two or more entries cut into two balanced parts
-// (a split line each), the others kept whole.
-void build_halves(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz,
-                  std::vector<int4> &seg, std::vector<int4> &split, SegTable &t) {
+// Host: every line of `parts` or more entries cut into that many balanced
+// parts (a split line each), the others kept whole.
+void build_cut(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz, int parts,
+               std::vector<int4> &seg, std::vector<int4> &split, SegTable &t) {
   seg.clear();
   split.clear();
   t.mean_len = nlines > 0 ? (double)nnz / (double)nlines : 0.0;
@@ -358,27 +358,29 @@ void build_halves(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz,
   for (int64_t l = 0; l < nlines; ++l) {
     const int64_t b = ptr[l], e = ptr[l + 1], len = e - b;
     t.max_len = std::max<int64_t>(t.max_len, len);
-    if (len < 2) {
+    if (len < parts) {
       seg.push_back(make_int4((int)l, (int)b, (int)e, -1));
       continue;
     }
     const int sid = (int)split.size();
-    split.push_back(make_int4((int)seg.size(), 2, (int)slots, 0));
-    slots += 2;
-    seg.push_back(make_int4((int)l, (int)b, (int)(b + len / 2), sid));
-    seg.push_back(make_int4((int)l, (int)(b + len / 2), (int)e, sid));
+    split.push_back(make_int4((int)seg.size(), parts, (int)slots, 0));
+    slots += parts;
+    for (int q = 0; q < parts; ++q)
+      seg.push_back(make_int4((int)l, (int)(b + q * len / parts), (int)(b + (q + 1) * len / parts),
+                              sid));
   }
   t.nseg = (int64_t)seg.size();
   t.nsplit = (int64_t)split.size();
   t.nslots = slots;
 }
 
-// Whether table t gets its halved copy: a large layer (2^21+ entries) of
-// long, evenly filled lines.  Measured on 10000 x 10000 at 90 % (1000
-// entries per line), 64-wide slices: forward 182 -> 159 us, dX 180 -> 157,
-// dW 187 -> 166.  Which slices walk the halves is decided per product at
-// launch (the SpMMs' combines cost more than they save on narrow slices:
-// batch 8 forward 44 -> 63 us).
+// Whether table t gets its cut copies (halves and thirds): a large layer
+// (2^21+ entries) of long, evenly filled lines.  Measured on 10000 x 10000
+// at 90 % (1000 entries per line), 64-wide slices: forward 182 -> 159 us
+// with halves, 148 with thirds; dX 180 -> 157 / 149; dW 187 -> 166 / 157.
+// Which slices walk which copy is decided per product at launch (the
+// SpMMs' combines cost more than they save on narrow slices: batch 8
+// forward 44 -> 63 us with halves).
 bool halves_pay(const SegTable &t, int64_t nnz) {
   return nnz >= (int64_t(1) << 21) && t.mean_len >= 400.0 && (double)t.max_len <= 8.0 * t.mean_len;
 }
@@ -455,17 +457,20 @@ snack_status finish_layout(Layer &L, const uint64_t *d_cell_key, cudaStream_t s,
   build_segments(cp, L.in, n, seg, split, L.csc);
   st = upload_segments(seg, split, L.csc, &L.device_bytes, s, err);
   if (st != SNACK_OK) return st;
-  free_segments(L.csr_half);
-  free_segments(L.csc_half);
-  if (halves_pay(L.csr, n)) {
-    build_halves(rp, L.out, n, seg, split, L.csr_half);
-    st = upload_segments(seg, split, L.csr_half, &L.device_bytes, s, err);
-    if (st != SNACK_OK) return st;
-  }
-  if (halves_pay(L.csc, n)) {
-    build_halves(cp, L.in, n, seg, split, L.csc_half);
-    st = upload_segments(seg, split, L.csc_half, &L.device_bytes, s, err);
-    if (st != SNACK_OK) return st;
+  for (SegTable *t : {&L.csr_half, &L.csc_half, &L.csr_third, &L.csc_third}) free_segments(*t);
+  for (int parts : {2, 3}) {
+    if (halves_pay(L.csr, n)) {
+      SegTable &t = parts == 2 ? L.csr_half : L.csr_third;
+      build_cut(rp, L.out, n, parts, seg, split, t);
+      st = upload_segments(seg, split, t, &L.device_bytes, s, err);
+      if (st != SNACK_OK) return st;
+    }
+    if (halves_pay(L.csc, n)) {
+      SegTable &t = parts == 2 ? L.csc_half : L.csc_third;
+      build_cut(cp, L.in, n, parts, seg, split, t);
+      st = upload_segments(seg, split, t, &L.device_bytes, s, err);
+      if (st != SNACK_OK) return st;
+    }
   }
   // Column-panel partition of the row table (large layers only; the panel
   // SDDMM runs over rows).
@@ -496,7 +501,7 @@ snack_status finish_layout(Layer &L, const uint64_t *d_cell_key, cudaStream_t s,
   L.d_counter = nullptr;
   TRY_CUDA(dev_alloc(&L.d_partial, partial_floats(L), &L.device_bytes));
   const int64_t tickets = std::max({L.csr.nsplit, L.csc.nsplit, L.csr_half.nsplit,
-                                    L.csc_half.nsplit});
+                                    L.csc_half.nsplit, L.csr_third.nsplit, L.csc_third.nsplit});
   TRY_CUDA(dev_alloc(&L.d_counter, (size_t)tickets, &L.device_bytes));
   TRY_CUDA(cudaMemsetAsync(L.d_counter, 0, std::max<size_t>(tickets, 1) * sizeof(int), s));
   TRY_CUDA(cudaStreamSynchronize(s));
@@ -901,6 +906,8 @@ snack_status prune_regrow(Layer &L, float frac, uint64_t seed, int64_t *pruned, 
   std::swap(L.csc, N.csc);
   std::swap(L.csr_half, N.csr_half);
   std::swap(L.csc_half, N.csc_half);
+  std::swap(L.csr_third, N.csr_third);
+  std::swap(L.csc_third, N.csc_third);
   std::swap(L.d_partial, N.d_partial);
   std::swap(L.d_counter, N.d_counter);
   L.csc_vals = !L.values_shared;  // the copy was derived from these values
@@ -921,7 +928,9 @@ snack_status refresh_csc_values(Layer &L, cudaStream_t s, std::string &err) {
 size_t partial_floats(const Layer &L) {
   return (size_t)std::max({L.csr.nslots * kMaxSlice, L.csc.nslots * kMaxSlice,
                            L.csr_half.nslots * kHalfLineWidth,
-                           L.csc_half.nslots * kHalfLineWidth});
+                           L.csc_half.nslots * kHalfLineWidth,
+                           L.csr_third.nslots * kHalfLineWidth,
+                           L.csc_third.nslots * kHalfLineWidth});
 }
 
 void free_layer(Layer &L) {
@@ -934,8 +943,7 @@ void free_layer(Layer &L) {
     if (p) cudaFree(p);
   free_panel_table(L.csr.panel);
   free_panel_table(L.csc.panel);
-  free_segments(L.csr_half);
-  free_segments(L.csc_half);
+  for (SegTable *t : {&L.csr_half, &L.csc_half, &L.csr_third, &L.csc_third}) free_segments(*t);
   L = Layer();
 }
 
