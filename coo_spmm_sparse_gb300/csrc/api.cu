@@ -71,13 +71,13 @@ void account(snack::Layer &L) {
   b += (size_t)L.nnz_pad * 4 * 5;  // col, row, val, csc_row, csc_perm
   b += (size_t)(L.out + 1 + L.in + 1) * 4;
   for (const snack::SegTable *t :
-       {&L.csr, &L.csc, &L.csr_half, &L.csc_half, &L.csr_third, &L.csc_third})
+       {&L.csr, &L.csc, &L.csr_half, &L.csc_half, &L.csr_wide, &L.csc_wide})
     b += (size_t)(t->nseg + t->nsplit) * sizeof(int4);
   b += L.csr.panel.bytes + L.csc.panel.bytes;
   b += (size_t)(L.in + L.out) * snack::kMaxSlice * 4;
   b += snack::partial_floats(L) * 4;
   b += (size_t)std::max({L.csr.nsplit, L.csc.nsplit, L.csr_half.nsplit, L.csc_half.nsplit,
-                         L.csr_third.nsplit, L.csc_third.nsplit}) *
+                         L.csr_wide.nsplit, L.csc_wide.nsplit}) *
        4;
   b += 4;  // error flag
   // column-ordered values; optimizer state, gradient buffer
@@ -101,17 +101,17 @@ snack_status finish_create(snack_layer *h, snack_status st, const std::string &e
 
 // The row (rows) or column table one product (SpMM or SDDMM) walks for a
 // slice of nb batch rows, where the cut copies are built: slices of
-// kHalfLineWidth walk the lines in thirds (10000 x 10000 at 90 %, batch 64:
-// forward / dX / dW 157 / 156 / 169 us with halves, 148 / 149 / 157 with
-// thirds; at 95 % dW 88 -> 84), 32-wide slices of the SDDMM in halves (its
-// entries need no combining: batch 32 dW at 90 % 123.9 -> 106.1 us, at 95 %
-// 66.3 -> 59.9; thirds 106.6 / 61.7, and the SpMMs lost there, 101.8 ->
-// 106.7 and 58.5 -> 59.3 with halves).
+// kHalfLineWidth walk the lines in kWideCutParts parts (10000 x 10000 at
+// 90 %, batch 64: forward / dX / dW 157 / 156 / 169 us in halves, 144 / 144
+// / 151 in quarters; at 95 % dW 88 -> 84), 32-wide slices of the SDDMM in
+// halves (its entries need no combining: batch 32 dW at 90 % 123.9 -> 106.1
+// us, at 95 % 66.3 -> 59.9; thirds 106.6 / 61.7, and the SpMMs lost there,
+// 101.8 -> 106.7 and 58.5 -> 59.3 with halves).
 const snack::SegTable &line_table(const snack::Layer &L, bool rows, int64_t nb, bool sddmm) {
   const snack::SegTable &half = rows ? L.csr_half : L.csc_half;
-  const snack::SegTable &third = rows ? L.csr_third : L.csc_third;
+  const snack::SegTable &wide = rows ? L.csr_wide : L.csc_wide;
   const int w = snack::slice_width(std::min<int64_t>(nb, snack::kMaxSlice));
-  if (w == snack::kHalfLineWidth && third.nseg > 0) return third;
+  if (w == snack::kHalfLineWidth && wide.nseg > 0) return wide;
   if (sddmm && w == 32 && half.nseg > 0) return half;
   return rows ? L.csr : L.csc;
 }

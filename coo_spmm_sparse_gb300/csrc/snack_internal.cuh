@@ -44,10 +44,12 @@ constexpr int kPanelLinesPerWarp = 4;  // lines one consumer warp can hold
 
 constexpr int kPanelWidths = 4;  // slices of 8, 16, 32, 64 floats
 
-// Widest slice that walks the cut-line tables (Layer::csr_half, csr_third):
+// Widest slice that walks the cut-line tables (Layer::csr_half, csr_wide):
 // at 64 floats per entry a team's walk of a long line is latency-bound, and
 // the last round of teams runs mostly empty.
 constexpr int kHalfLineWidth = 64;
+// Parts per line of the cut copy that slices of kHalfLineWidth walk.
+constexpr int kWideCutParts = 4;
 
 struct PanelTable {
   int4 *d_part = nullptr;  // [ctas][32]
@@ -87,10 +89,10 @@ struct Layer {
   bool values_shared = false;      // a writable values pointer is out (snack_values)
   int32_t *d_col_ptr = nullptr;
   SegTable csr, csc;
-  // The same lines cut into two (and three) balanced parts each, for wide
-  // slices on layers of 2^21+ entries whose lines average 400+ entries
-  // (nseg 0 when not built).
-  SegTable csr_half, csc_half, csr_third, csc_third;
+  // The same lines cut into 2 (half) and kWideCutParts (wide) balanced parts
+  // each, for wide slices on layers of 2^21+ entries whose lines average
+  // 400+ entries (nseg 0 when not built).
+  SegTable csr_half, csc_half, csr_wide, csc_wide;
   // workspace
   float *d_xt = nullptr;       // [in][kMaxSlice]   transposed X slice
   float *d_dyt = nullptr;      // [out][kMaxSlice]  transposed dY slice

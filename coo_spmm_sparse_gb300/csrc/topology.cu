@@ -374,12 +374,13 @@ void build_cut(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz, int
   t.nslots = slots;
 }
 
-// Whether table t gets its cut copies (halves and thirds): a large layer
+// Whether table t gets its cut copies (halves and quarters): a large layer
 // (2^21+ entries) of long, evenly filled lines.  Measured on 10000 x 10000
-// at 90 % (1000 entries per line), 64-wide slices: forward 182 -> 159 us
-// with halves, 148 with thirds; dX 180 -> 157 / 149; dW 187 -> 166 / 157.
-// Which slices walk which copy is decided per product at launch (the
-// SpMMs' combines cost more than they save on narrow slices: batch 8
+// at 90 % (1000 entries per line), 64-wide slices, forward 182 us with whole
+// lines, 159 / 148 / 144 / 146 with 2 / 3 / 4 / 5 parts; dW 187 -> 166 /
+// 157 / 151 / 149 (the fifth part lost on the forward and on the 95 %
+// layer).  Which slices walk which copy is decided per product at launch
+// (the SpMMs' combines cost more than they save on narrow slices: batch 8
 // forward 44 -> 63 us with halves).
 bool halves_pay(const SegTable &t, int64_t nnz) {
   return nnz >= (int64_t(1) << 21) && t.mean_len >= 400.0 && (double)t.max_len <= 8.0 * t.mean_len;
@@ -457,16 +458,16 @@ snack_status finish_layout(Layer &L, const uint64_t *d_cell_key, cudaStream_t s,
   build_segments(cp, L.in, n, seg, split, L.csc);
   st = upload_segments(seg, split, L.csc, &L.device_bytes, s, err);
   if (st != SNACK_OK) return st;
-  for (SegTable *t : {&L.csr_half, &L.csc_half, &L.csr_third, &L.csc_third}) free_segments(*t);
-  for (int parts : {2, 3}) {
+  for (SegTable *t : {&L.csr_half, &L.csc_half, &L.csr_wide, &L.csc_wide}) free_segments(*t);
+  for (int parts : {2, kWideCutParts}) {
     if (halves_pay(L.csr, n)) {
-      SegTable &t = parts == 2 ? L.csr_half : L.csr_third;
+      SegTable &t = parts == 2 ? L.csr_half : L.csr_wide;
       build_cut(rp, L.out, n, parts, seg, split, t);
       st = upload_segments(seg, split, t, &L.device_bytes, s, err);
       if (st != SNACK_OK) return st;
     }
     if (halves_pay(L.csc, n)) {
-      SegTable &t = parts == 2 ? L.csc_half : L.csc_third;
+      SegTable &t = parts == 2 ? L.csc_half : L.csc_wide;
       build_cut(cp, L.in, n, parts, seg, split, t);
       st = upload_segments(seg, split, t, &L.device_bytes, s, err);
       if (st != SNACK_OK) return st;
@@ -501,7 +502,7 @@ snack_status finish_layout(Layer &L, const uint64_t *d_cell_key, cudaStream_t s,
   L.d_counter = nullptr;
   TRY_CUDA(dev_alloc(&L.d_partial, partial_floats(L), &L.device_bytes));
   const int64_t tickets = std::max({L.csr.nsplit, L.csc.nsplit, L.csr_half.nsplit,
-                                    L.csc_half.nsplit, L.csr_third.nsplit, L.csc_third.nsplit});
+                                    L.csc_half.nsplit, L.csr_wide.nsplit, L.csc_wide.nsplit});
   TRY_CUDA(dev_alloc(&L.d_counter, (size_t)tickets, &L.device_bytes));
   TRY_CUDA(cudaMemsetAsync(L.d_counter, 0, std::max<size_t>(tickets, 1) * sizeof(int), s));
   TRY_CUDA(cudaStreamSynchronize(s));
@@ -906,8 +907,8 @@ snack_status prune_regrow(Layer &L, float frac, uint64_t seed, int64_t *pruned, 
   std::swap(L.csc, N.csc);
   std::swap(L.csr_half, N.csr_half);
   std::swap(L.csc_half, N.csc_half);
-  std::swap(L.csr_third, N.csr_third);
-  std::swap(L.csc_third, N.csc_third);
+  std::swap(L.csr_wide, N.csr_wide);
+  std::swap(L.csc_wide, N.csc_wide);
   std::swap(L.d_partial, N.d_partial);
   std::swap(L.d_counter, N.d_counter);
   L.csc_vals = !L.values_shared;  // the copy was derived from these values
@@ -929,8 +930,8 @@ size_t partial_floats(const Layer &L) {
   return (size_t)std::max({L.csr.nslots * kMaxSlice, L.csc.nslots * kMaxSlice,
                            L.csr_half.nslots * kHalfLineWidth,
                            L.csc_half.nslots * kHalfLineWidth,
-                           L.csr_third.nslots * kHalfLineWidth,
-                           L.csc_third.nslots * kHalfLineWidth});
+                           L.csr_wide.nslots * kHalfLineWidth,
+                           L.csc_wide.nslots * kHalfLineWidth});
 }
 
 void free_layer(Layer &L) {
@@ -943,7 +944,7 @@ void free_layer(Layer &L) {
     if (p) cudaFree(p);
   free_panel_table(L.csr.panel);
   free_panel_table(L.csc.panel);
-  for (SegTable *t : {&L.csr_half, &L.csc_half, &L.csr_third, &L.csc_third}) free_segments(*t);
+  for (SegTable *t : {&L.csr_half, &L.csc_half, &L.csr_wide, &L.csc_wide}) free_segments(*t);
   L = Layer();
 }
 

@@ -23,10 +23,10 @@ def test_handle_bytes_follow_nnz(sparsity):
     acct = m.snack_device_bytes(h)
     # indices, values in both orders and both layouts: 24 B per stored
     # entry, plus per line an offset, a segment record and a 256-float row of
-    # operand workspace, and on a large layer of long lines its halved and
-    # third-cut copies (5 segment records and 2 split records per line, the
-    # thirds' partial sums of 64 floats each, two tickets)
-    per_line = 4 + 16 + 256 * 4 + 5 * 16 + 2 * 16 + 3 * 64 * 4 + 2 * 4
+    # operand workspace, and on a large layer of long lines its copies cut
+    # in 2 and 4 parts (6 segment records and 2 split records per line, the
+    # quarters' partial sums of 64 floats each, two tickets)
+    per_line = 4 + 16 + 256 * 4 + 6 * 16 + 2 * 16 + 4 * 64 * 4 + 2 * 4
     assert 24 * nnz <= acct <= 25 * nnz + per_line * (out + inp) + (1 << 20)
     # what the device really gave up (allocation granularity included)
     assert free0 - free1 <= acct + (64 << 20)

@@ -313,7 +313,7 @@ def test_heavy_tailed_rows_with_empty_rows():
 
 def test_halved_lines_wide_slices():
     # 2.2 M entries over 4096 x 4096 (537 per row and column): 64-wide
-    # slices walk every line in three parts, 32-wide slices of the weight
+    # slices walk every line in four parts, 32-wide slices of the weight
     # product and of the fused backward in two, combined by the split-line
     # path; every product, the fused backward included, against the oracle
     out = inp = 4096
@@ -321,8 +321,8 @@ def test_halved_lines_wide_slices():
     row, col, _ = sn().snack_export(h0)
     val = np.random.default_rng(32).standard_normal(row.size).astype(np.float32)
     h, ref = _layer_case(out, inp, row, col, val, [64, 41, 100, 32, 16], seed=33)
-    assert sn().snack_plan(h, 0, 64)[2] == 3 * out
-    assert sn().snack_plan(h, 1, 64)[2] == 3 * inp
+    assert sn().snack_plan(h, 0, 64)[2] == 4 * out
+    assert sn().snack_plan(h, 1, 64)[2] == 4 * inp
     assert sn().snack_plan(h, 2, 32)[2] == 2 * out
     # the halves' tickets re-arm: identical bits on a second call
     X = to_dev(np.random.default_rng(34).standard_normal((64, inp)).astype(np.float32))
@@ -451,11 +451,11 @@ def test_plan_follows_batch_and_row_length():
     # with a slice of w (the remainder follows as its own slice)
     for B, w in ((9, 16), (33, 32), (40, 32), (41, 64), (65, 64), (129, 128), (300, 256)):
         assert sn().snack_plan(h5, 0, B)[0] == w, B
-    # 64-wide slices of a large layer of long lines walk its lines in thirds
-    # (three segments per row or column), 32-wide slices of the weight
+    # 64-wide slices of a large layer of long lines walk its lines in four
+    # parts (four segments per row or column), 32-wide slices of the weight
     # product in halves; other widths and small layers walk whole lines
     for op in (0, 1, 2):
-        assert sn().snack_plan(h5, op, 64)[2] == 3 * L.out
+        assert sn().snack_plan(h5, op, 64)[2] == 4 * L.out
         assert sn().snack_plan(h5, op, 32)[2] == (2 * L.out if op == 2 else L.out)
         assert sn().snack_plan(h5, op, 16)[2] == L.out
         assert sn().snack_plan(h5, op, 128)[2] == L.out
