@@ -103,7 +103,10 @@ snack_status finish_create(snack_layer *h, snack_status st, const std::string &e
 // slice of nb batch rows, where the cut copies are built: slices of
 // kHalfLineWidth walk the lines in kWideCutParts parts (10000 x 10000 at
 // 90 %, batch 64: forward / dX / dW 157 / 156 / 169 us in halves, 144 / 144
-// / 151 in quarters; at 95 % dW 88 -> 84), 32-wide slices of the SDDMM in
+// / 151 in quarters; at 95 % dW 88 -> 84), and so do the SDDMM's wider
+// slices (its entries need no partial sums; batch 128 / 256 dW at 90 % 356
+// / 669 -> 277 / 573 us, at 95 % 181 / 348 -> 151 / 302; the SpMMs' partial
+// sums are sized for 64-float slices), 32-wide slices of the SDDMM in
 // halves (its entries need no combining: batch 32 dW at 90 % 123.9 -> 106.1
 // us, at 95 % 66.3 -> 59.9; thirds 106.6 / 61.7, and the SpMMs lost there,
 // 101.8 -> 106.7 and 58.5 -> 59.3 with halves).
@@ -111,7 +114,8 @@ const snack::SegTable &line_table(const snack::Layer &L, bool rows, int64_t nb, 
   const snack::SegTable &half = rows ? L.csr_half : L.csc_half;
   const snack::SegTable &wide = rows ? L.csr_wide : L.csc_wide;
   const int w = snack::slice_width(std::min<int64_t>(nb, snack::kMaxSlice));
-  if (w == snack::kHalfLineWidth && wide.nseg > 0) return wide;
+  if (wide.nseg > 0 && (w == snack::kHalfLineWidth || (sddmm && w > snack::kHalfLineWidth)))
+    return wide;
   if (sddmm && w == 32 && half.nseg > 0) return half;
   return rows ? L.csr : L.csc;
 }

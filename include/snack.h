@@ -249,8 +249,9 @@ snack_status snack_export_segments(snack_handle h, int32_t *row_ptr, int32_t *co
  * share one row (or column) segment (the launch may halve them when that
  * keeps every segment in one wave of resident teams), the number of
  * segments (on layers of 2^21+ entries whose lines average 400+ entries,
- * 64-wide slices walk every line in four parts and 32-wide slices of op 2
- * in two, so four or two times the lines), and where the dense operand is
+ * 64-wide slices and the wider ones of op 2 walk every line in four parts
+ * and 32-wide slices of op 2 in two, so four or two times the lines), and
+ * where the dense operand is
  * gathered from: 0 = global memory
  * (through L1), 1 = a copy of the whole operand in every block's shared
  * memory, 2 = shared memory one column panel at a time (the column-panel

@@ -320,7 +320,7 @@ def test_halved_lines_wide_slices():
     h0, _ = sn().snack_create_random(out, inp, 2_200_000, 31)
     row, col, _ = sn().snack_export(h0)
     val = np.random.default_rng(32).standard_normal(row.size).astype(np.float32)
-    h, ref = _layer_case(out, inp, row, col, val, [64, 41, 100, 32, 16], seed=33)
+    h, ref = _layer_case(out, inp, row, col, val, [64, 41, 100, 200, 32, 16], seed=33)
     assert sn().snack_plan(h, 0, 64)[2] == 4 * out
     assert sn().snack_plan(h, 1, 64)[2] == 4 * inp
     assert sn().snack_plan(h, 2, 32)[2] == 2 * out
@@ -452,13 +452,14 @@ def test_plan_follows_batch_and_row_length():
     for B, w in ((9, 16), (33, 32), (40, 32), (41, 64), (65, 64), (129, 128), (300, 256)):
         assert sn().snack_plan(h5, 0, B)[0] == w, B
     # 64-wide slices of a large layer of long lines walk its lines in four
-    # parts (four segments per row or column), 32-wide slices of the weight
-    # product in halves; other widths and small layers walk whole lines
+    # parts (four segments per row or column), and so do the weight
+    # product's wider slices; its 32-wide slices walk halves; other widths
+    # and small layers walk whole lines
     for op in (0, 1, 2):
         assert sn().snack_plan(h5, op, 64)[2] == 4 * L.out
         assert sn().snack_plan(h5, op, 32)[2] == (2 * L.out if op == 2 else L.out)
         assert sn().snack_plan(h5, op, 16)[2] == L.out
-        assert sn().snack_plan(h5, op, 128)[2] == L.out
+        assert sn().snack_plan(h5, op, 128)[2] == (4 * L.out if op == 2 else L.out)
     assert sn().snack_plan(h, 0, 64)[2] == L.out
     small = workloads.workload("toy256").layers[0]
     r, c, v = small.coo()
