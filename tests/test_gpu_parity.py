@@ -324,12 +324,25 @@ def test_halved_lines_wide_slices():
     assert sn().snack_plan(h, 0, 64)[2] == 4 * out
     assert sn().snack_plan(h, 1, 64)[2] == 4 * inp
     assert sn().snack_plan(h, 2, 32)[2] == 2 * out
-    # the halves' tickets re-arm: identical bits on a second call
+    # the parts' partial sums are summed again from scratch: identical bits on
+    # a second call
     X = to_dev(np.random.default_rng(34).standard_normal((64, inp)).astype(np.float32))
     Y1 = sn().snack_forward(h, X)
     Y2 = sn().snack_forward(h, X)
     torch.cuda.synchronize()
     assert torch.equal(Y1, Y2)
+    # the cut copies are rebuilt with the topology
+    pruned, trials = sn().snack_prune_regrow(h, 0.2, 35)
+    o = oracle.prune_regrow(out, inp, ref["row"], ref["col"], ref["val"], 0.2, 35)
+    assert (pruned, trials) == (o["pruned"], o["trials"])
+    ref2 = canonical(out, inp, o["row"], o["col"], o["val"])
+    check_topology(h, ref2)
+    assert sn().snack_plan(h, 0, 64)[2] == 4 * out
+    g = np.random.default_rng(36)
+    for B in (64, 32):
+        Xb = g.standard_normal((B, inp)).astype(np.float32)
+        dY = g.standard_normal((B, out)).astype(np.float32)
+        check_products(h, out, inp, ref2, Xb, dY)
 
 
 def test_identity_pattern_bit_exact():
