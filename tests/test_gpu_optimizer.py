@@ -143,7 +143,10 @@ def test_sgd_plain_and_momentum(B):
 @pytest.mark.parametrize("shape,B", [((256, 256, 90), 4), ((3072, 768, 95), 1),
                                      ((3072, 768, 95), 8), ((768, 3072, 95), 32),
                                      ((3000, 3000, 85), 64), ((700, 900, 80), 130),
-                                     ((700, 900, 80), 300)])
+                                     ((700, 900, 80), 300),
+                                     # 2.3 M entries, 960 per line: the gradient of
+                                     # 64- and 128-wide slices over lines cut in four
+                                     ((2400, 2400, 60), 64), ((2400, 2400, 60), 130)])
 def test_adam_steps(shape, B):
     c = _uniform_case(*shape, 31)
     for t in (1, 2, 3):
