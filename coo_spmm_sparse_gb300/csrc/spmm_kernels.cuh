@@ -575,7 +575,46 @@ __device__ __forceinline__ void load_col_step(const int32_t *col, int kb, int k1
 
 // dW for up to two quads of one group (columns already loaded): the G lanes
 // of a group each form part of the batch dot product and meet by shuffle.
-template <int BW, bool SM, bool OPT>
+// dW of one quad when its four dot products are spread over a group of G
+// >= 2 lanes (d[e]: this lane's part of entry e): a butterfly over the
+// group sums them and leaves one entry per lane at once.  The first level
+// keeps entries 2-3 on the upper half of the group and 0-1 on the lower
+// (two shuffles), the second one entry per lane (one shuffle), the rest
+// finish that entry's sum; 2 / 3 / 4 / 5 / 6 shuffles per quad at G = 2 /
+// 4 / 8 / 16 / 32, against log2(G) per entry when each entry is summed on
+// its own (the shuffles go through the L1 data pipe the gathers need: at
+// 64-wide slices they were 0.86 of its 3.6 wavefronts per entry).  With G
+// = 2 each lane ends with two entries.
+template <int G>
+__device__ __forceinline__ void sddmm_store_spread(const SddmmArgs &a, int kq, int k0, int k1,
+                                                   int sub, unsigned gmask, float (&d)[4]) {
+  const bool up = (sub & (G / 2)) != 0;
+  const float s0 = __shfl_xor_sync(gmask, up ? d[0] : d[2], G / 2);
+  const float s1 = __shfl_xor_sync(gmask, up ? d[1] : d[3], G / 2);
+  d[0] = (up ? d[2] : d[0]) + s0;
+  d[1] = (up ? d[3] : d[1]) + s1;
+  const int base = kq + (up ? 2 : 0);
+  if constexpr (G == 2) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      if (base + e >= k0 && base + e < k1) {
+        float *p = a.dw + base + e;
+        *p = a.accumulate ? *p + d[e] : d[e];
+      }
+  } else {
+    const bool up2 = (sub & (G / 4)) != 0;
+    float r = (up2 ? d[1] : d[0]) + __shfl_xor_sync(gmask, up2 ? d[0] : d[1], G / 4);
+#pragma unroll
+    for (int off = G / 8; off >= 1; off >>= 1) r += __shfl_xor_sync(gmask, r, off);
+    const int k = base + (up2 ? 1 : 0);
+    if ((sub & (G / 4 - 1)) == 0 && k >= k0 && k < k1) {
+      float *p = a.dw + k;
+      *p = a.accumulate ? *p + r : r;
+    }
+  }
+}
+
+template <int BW, bool SM, bool OPT, bool SPREAD>
 __device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt, int kb, int k0,
                                             int k1, int npt, unsigned gmask, int sub,
                                             const float (&dy)[SliceShape<BW>::NV]
@@ -622,9 +661,15 @@ __device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt,
       for (int v = 0; v < NV; ++v)
 #pragma unroll
         for (int i = 0; i < VEC; ++i) s = fmaf(dy[v][i], x[q][e][v][i], s);
+      if constexpr (OPT || !SPREAD) {
 #pragma unroll
-      for (int off = 1; off < G; off <<= 1) s += __shfl_xor_sync(gmask, s, off);
+        for (int off = 1; off < G; off <<= 1) s += __shfl_xor_sync(gmask, s, off);
+      }
       res[e] = s;
+    }
+    if constexpr (SPREAD && !OPT && G >= 2) {
+      sddmm_store_spread<G>(a, kq, k0, k1, sub, gmask, res);
+      continue;
     }
     if (sub == 0) {
       if constexpr (OPT) {
@@ -706,8 +751,8 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, 
     for (; kb < k1; kb += 4 * QPS * npt) {
       int cn[2][4] = {};
       load_col_step<QPS>(a.col, kb + 4 * QPS * npt, k1, npt, cn);
-      sddmm_quads<BW, SM, OPT>(a, xt, kb, k0, k1, npt, gmask, sub, dy, c,
-                               QPS == 2 && kb + 4 * npt < k1);
+      sddmm_quads<BW, SM, OPT, !(FUSED && BW >= 64)>(a, xt, kb, k0, k1, npt, gmask, sub, dy, c,
+                                                     QPS == 2 && kb + 4 * npt < k1);
 #pragma unroll
       for (int q = 0; q < 2; ++q)
 #pragma unroll
