@@ -513,7 +513,8 @@ def run_ours(args):
 
     def time_e2e(run):
         """Milliseconds of args.steps e2e steps (max over ranks), each after
-        an L2 flush, between events on `stream`."""
+        an L2 flush, between events on `stream`; also this rank's per-step
+        times (the host link is shared, so single steps can stall)."""
         evs = []
         barrier()
         with torch.cuda.stream(stream):
@@ -526,13 +527,14 @@ def run_ours(args):
                 evs.append((e0, e1))
         torch.cuda.synchronize()
         barrier()
-        return reduce_max(sum(a.elapsed_time(b) for a, b in evs), dev)
+        per = [a.elapsed_time(b) for a, b in evs]
+        return reduce_max(sum(per), dev), per
 
     with torch.cuda.stream(stream):
         for _ in range(3):
             e2e_step()
     torch.cuda.synchronize()
-    eager_ms = time_e2e(e2e_step)
+    eager_ms, _ = time_e2e(e2e_step)
     # The same pipeline (its copies, events and library calls) captured once
     # and replayed from a CUDA graph, as the device-resident step is: every
     # replay moves the step's inputs and results between pinned host memory
@@ -545,7 +547,7 @@ def run_ours(args):
             e2e_graph.replay()
     torch.cuda.synchronize()
     h_out.zero_()  # what the check below reads must come from the timed replays
-    e2e_ms = time_e2e(e2e_graph.replay)
+    e2e_ms, e2e_per = time_e2e(e2e_graph.replay)
     del e2e_graph
     # The host buffer holds the last step's results: one pair's Y must equal
     # a forward of the same (device-resident) X with the current values (the
@@ -586,6 +588,8 @@ def run_ours(args):
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
                     "eager_value": round(eager_value, 2),
+                    "ms_per_step_min_median_max": [round(x, 4) for x in (
+                        min(e2e_per), sorted(e2e_per)[len(e2e_per) // 2], max(e2e_per))],
                     "how": "per step and per layer/batch: pinned H2D copy of its X and dY "
                            "(one copy stream), snack_forward + snack_backward via the C ABI "
                            "once they have landed, D2H copy of its Y, dX, dW on a second copy "
