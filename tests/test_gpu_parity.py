@@ -53,6 +53,17 @@ def test_toy256_all_batch_widths():
     _layer_case(L.out, L.inp, row, col, val, ALL_B, seed=1)
 
 
+def test_slices_after_the_first_accumulate_at_every_group_size():
+    """Batches past the widest slice (256) run further slices that add into
+    dW: remainders of 2 / 8 / 16 / 32 / 74 / 256 rows take slices of 2, 8,
+    16, 32, 128 and 256 floats, so every lane-group size of the weight
+    product's reduction (1, 2, 4, 8, 16, 32 lanes per entry) stores
+    through its accumulate path."""
+    L = workloads.workload("toy256").layers[0]
+    row, col, val = L.coo()
+    _layer_case(L.out, L.inp, row, col, val, [258, 264, 272, 288, 330, 512], seed=11)
+
+
 @pytest.mark.parametrize("which", [0, 1])
 def test_gpt2_mlp_layers(which):
     L = workloads.workload("gpt2_mlp").layers[which]
