@@ -762,31 +762,59 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, 
 }
 
 // Second pass of an SpMM whose split lines only parked their parts'
-// partials (launched with a.counter null): warp w sums split line w's parts
-// in part order and writes the line's outputs.  Its grid-dependency wait
+// partials (launched with a.counter null): each thread takes VEC batch rows
+// of one split line (BW / VEC threads per line, so a 64-wide slice's 10000
+// lines fit one wave), loads eight parts at once and adds them in part
+// order, then writes the line's outputs.  Its grid-dependency wait
 // makes the first pass's partials visible.
 template <int BW>
+__host__ __device__ constexpr int split_sum_vec() {
+  return BW >= 4 ? 4 : BW;
+}
+
+template <int BW>
 __global__ void __launch_bounds__(256) split_sums(const SpmmArgs a, int64_t nsplit) {
+  constexpr int VEC = split_sum_vec<BW>(), TPL = BW / VEC;
   griddep_wait();
-  const int64_t w = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
-  if (w >= nsplit) return;
-  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  const int64_t w = t / TPL;
+  const int b0 = (int)(t % TPL) * VEC;
+  if (w >= nsplit || b0 >= a.nb) return;
   const int4 sp = a.split[w];
   const int line = a.seg[sp.x].x;
-  for (int b = lane; b < BW && b < a.nb; b += 32) {
-    const float *q = a.partial + (int64_t)sp.z * BW + b;
-    float t = 0.f;
-    int p = 0;
-    for (; p + 8 <= sp.y; p += 8) {
-      float x[8];
+  const float *q = a.partial + (int64_t)sp.z * BW + b0;
+  float s[VEC];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) x[u] = __ldcg(q + (int64_t)(p + u) * BW);
+  for (int i = 0; i < VEC; ++i) s[i] = 0.f;
+  for (int p = 0; p < sp.y; p += 8) {
+    float x[8][VEC];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) t += x[u];
+    for (int u = 0; u < 8; ++u) {
+      // past the last part: load the last part again (no branch, so all
+      // eight loads issue together) and leave it out of the sum
+      const float *r = q + (int64_t)min(p + u, sp.y - 1) * BW;
+      if constexpr (VEC == 4) {
+        const float4 f = __ldcg(reinterpret_cast<const float4 *>(r));
+        x[u][0] = f.x;
+        x[u][1] = f.y;
+        x[u][2] = f.z;
+        x[u][3] = f.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) x[u][i] = __ldcg(r + i);
+      }
     }
-    for (; p < sp.y; ++p) t += __ldcg(q + (int64_t)p * BW);
-    a.dst[(int64_t)b * a.ld + line] = t;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (p + u < sp.y) {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) s[i] += x[u][i];
+      }
   }
+  float *d = a.dst + (int64_t)b0 * a.ld + line;
+#pragma unroll
+  for (int i = 0; i < VEC; ++i)
+    if (b0 + i < a.nb) d[(int64_t)i * a.ld] = s[i];
 }
 
 template <int BW, int LPS, bool PERM>

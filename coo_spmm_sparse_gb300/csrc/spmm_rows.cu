@@ -17,7 +17,9 @@ cudaError_t launch_spmm_rows(const Plan &p, const SpmmArgs &args, bool pdl, cuda
 cudaError_t launch_split_sums(int bw, const SpmmArgs &a, int64_t nsplit, bool pdl,
                               cudaStream_t s) {
   if (nsplit == 0) return cudaSuccess;
-  const int64_t blocks = (nsplit * 32 + 255) / 256;
+  if (bw < 1 || bw > kMaxSlice) return cudaErrorInvalidValue;
+  const int64_t threads = nsplit * (bw / (bw >= 4 ? 4 : bw));  // split_sum_vec
+  const int64_t blocks = (threads + 255) / 256;
   switch (bw) {
     case 1: return launch_ex(split_sums<1>, blocks, pdl, s, a, nsplit);
     case 2: return launch_ex(split_sums<2>, blocks, pdl, s, a, nsplit);
