@@ -282,7 +282,9 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
   // 64: 90 % 307.6 -> 285.7 us, 95 % 157.8 -> 154.1; batch 32: 90 % 194.6 ->
   // 181.9, 95 % 102.5 -> 102.9; batch 16 lost (90 % 116.8 -> 126.7), and so
   // did halving only the rows at batch 32 (194.6 -> 227.8); thirds measured
-  // the same at batch 64 and slower at 32 (95 %: 101.4 -> 107.0).
+  // the same at batch 64 and slower at 32 (95 %: 101.4 -> 107.0), and
+  // quarters at batch 64 split the layers (90 % 285.8 -> 284.4, 95 % 152.1 ->
+  // 156.2).
   const bool both = dX && dW;
   const int w = snack::slice_width(std::min<int64_t>(nb, snack::kMaxSlice));
   const bool fused_halves = both && w >= 32 && w <= snack::kHalfLineWidth &&
