@@ -204,7 +204,7 @@ cudaError_t launch_cols(const snack::SegTable &t, const snack::Plan &p, snack::S
       a.perm ? snack::launch_spmm_cols(q, a, true, s) : snack::launch_spmm_rows(q, a, true, s);
   if (e != cudaSuccess || !two) return e;
   g_launches.fetch_add(1, std::memory_order_relaxed);  // the first; the caller counts the second
-  return snack::launch_split_sums(q.bw, a, t.nsplit, true, s);
+  return snack::launch_split_sums(q.bw, a, t.nsplit, t.max_parts, true, s);
 }
 
 // Rows of the next batch slice when `left` rows remain: at most kMaxSlice.
@@ -257,7 +257,7 @@ snack_status run_forward(snack_handle h, const float *X, float *Y, int64_t batch
       e = snack::launch_spmm_rows(q, a, true, s);
       if (e == cudaSuccess && two) {
         g_launches.fetch_add(1, std::memory_order_relaxed);
-        e = snack::launch_split_sums(q.bw, a, t.nsplit, true, s);
+        e = snack::launch_split_sums(q.bw, a, t.nsplit, t.max_parts, true, s);
       }
     }
     if (e != cudaSuccess) return cuda_fail(h, e, "forward launch");
@@ -389,7 +389,7 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     e = snack::launch_backward_fused(pc, cols, pr, rows, true, s);
     if (e == cudaSuccess && two) {
       g_launches.fetch_add(1, std::memory_order_relaxed);
-      e = snack::launch_split_sums(pc.bw, cols, tc.nsplit, true, s);
+      e = snack::launch_split_sums(pc.bw, cols, tc.nsplit, tc.max_parts, true, s);
     }
   } else if (dX)
     e = launch_cols(tc, pc, cols, nb, s);

@@ -69,6 +69,7 @@ struct SegTable {
   int64_t nslots = 0;      // partial-sum slots (sum of parts over split lines)
   double mean_len = 0.0;   // mean entries per line
   int64_t max_len = 0;     // longest line
+  int max_parts = 0;       // most parts of one split line
   int4 *d_seg = nullptr;   // [nseg]
   int4 *d_split = nullptr; // [nsplit]
   PanelTable panel;        // column-panel partition (d_part null when not built)
@@ -191,8 +192,8 @@ cudaError_t launch_spmm_rows(const Plan &p, const SpmmArgs &a, bool pdl, cudaStr
 cudaError_t launch_spmm_cols(const Plan &p, const SpmmArgs &a, bool pdl, cudaStream_t s);
 // Second pass summing the split lines' partials of an SpMM launched with
 // a.counter null (bw = that launch's slice width).
-cudaError_t launch_split_sums(int bw, const SpmmArgs &a, int64_t nsplit, bool pdl,
-                              cudaStream_t s);
+cudaError_t launch_split_sums(int bw, const SpmmArgs &a, int64_t nsplit, int max_parts,
+                              bool pdl, cudaStream_t s);
 cudaError_t launch_sddmm(const Plan &p, const SddmmArgs &a, bool pdl, cudaStream_t s);
 // The same with the optimizer step of a.opt applied instead of writing dW.
 cudaError_t launch_sddmm_step(const Plan &p, const SddmmArgs &a, bool pdl, cudaStream_t s);

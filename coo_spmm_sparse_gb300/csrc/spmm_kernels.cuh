@@ -454,19 +454,44 @@ __device__ __forceinline__ void spmm_part(const SpmmArgs &a, const float *op, in
     __threadfence();
     // The team's npt groups each sum the parts grp, grp + npt, ... in order,
     // then meet by shuffle: a fixed order for a given plan (reproducible),
-    // with up to npt parts' loads in flight at once.
+    // with up to npt parts' loads in flight at once.  The SpMM kernels of
+    // slices of 1-4 floats (where the tickets stay in use) load four of a
+    // group's parts at once: past the last part a group loads the last again
+    // and leaves it out of the sum.  (Wider kernels and the fused backward
+    // keep one part per load: the four would cost their main loop
+    // registers.)
     float tot[NV][VEC];
 #pragma unroll
     for (int v = 0; v < NV; ++v)
 #pragma unroll
       for (int i = 0; i < VEC; ++i) tot[v][i] = 0.f;
+    if constexpr (BW <= 4 && PIPE) {
 #pragma unroll 1
-    for (int p = grp; p < sp.y; p += npt) {
-      const float *q = a.partial + (int64_t)(sp.z + p) * BW + sub * VEC;
+      for (int p = grp; p < sp.y; p += 4 * npt) {
+        float x[4][VEC];
 #pragma unroll
-      for (int v = 0; v < NV; ++v)
+        for (int u = 0; u < 4; ++u) {
+          const float *q =
+              a.partial + (int64_t)(sp.z + min(p + u * npt, sp.y - 1)) * BW + sub * VEC;
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) tot[v][i] += __ldcg(q + v * G * VEC + i);
+          for (int i = 0; i < VEC; ++i) x[u][i] = __ldcg(q + i);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (p + u * npt < sp.y) {
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) tot[0][i] += x[u][i];
+          }
+      }
+    } else {
+#pragma unroll 1
+      for (int p = grp; p < sp.y; p += npt) {
+        const float *q = a.partial + (int64_t)(sp.z + p) * BW + sub * VEC;
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) tot[v][i] += __ldcg(q + v * G * VEC + i);
+      }
     }
 #pragma unroll
     for (int off = G; off < lps; off <<= 1)
@@ -762,56 +787,67 @@ __device__ __forceinline__ void sddmm_part(const SddmmArgs &a, const float *op, 
 }
 
 // Second pass of an SpMM whose split lines only parked their parts'
-// partials (launched with a.counter null): each thread takes VEC batch rows
-// of one split line (BW / VEC threads per line, so a 64-wide slice's 10000
-// lines fit one wave), loads eight parts at once and adds them in part
-// order, then writes the line's outputs.  Its grid-dependency wait
-// makes the first pass's partials visible.
+// partials (launched with a.counter null).  Each split line takes TPL x pl
+// threads: TPL = BW / VEC over its batch rows (VEC rows each) times pl over
+// its parts, thread j of those adding parts j, j + pl, ... in order, eight
+// loads at once (past the last part it loads the last again and leaves it
+// out of the sum).  pl = 1 for lines of a few parts, so a 64-wide slice's
+// 10000 quartered lines fit one wave; lines of many parts (the parts of a
+// heavy-tailed table's longest lines) take up to a warp, their pl sums
+// meeting by a butterfly of shuffles (a fixed order).  Its grid-dependency
+// wait makes the first pass's partials visible.
 template <int BW>
 __host__ __device__ constexpr int split_sum_vec() {
   return BW >= 4 ? 4 : BW;
 }
 
 template <int BW>
-__global__ void __launch_bounds__(256) split_sums(const SpmmArgs a, int64_t nsplit) {
+__global__ void __launch_bounds__(256) split_sums(const SpmmArgs a, int64_t nsplit, int pl) {
   constexpr int VEC = split_sum_vec<BW>(), TPL = BW / VEC;
   griddep_wait();
+  const int tpl = TPL * pl;  // a power of two; at most 32 when pl > 1
   const int64_t t = (int64_t)blockIdx.x * 256 + threadIdx.x;
-  const int64_t w = t / TPL;
-  const int b0 = (int)(t % TPL) * VEC;
-  if (w >= nsplit || b0 >= a.nb) return;
-  const int4 sp = a.split[w];
-  const int line = a.seg[sp.x].x;
-  const float *q = a.partial + (int64_t)sp.z * BW + b0;
+  const int64_t w = t / tpl;
+  const int r = (int)(t % tpl);
+  const int b0 = (r % TPL) * VEC;
+  const int j = r / TPL;
+  const bool live = w < nsplit && b0 < a.nb;
+  // With pl > 1 every lane of the warp meets the shuffles below: the lanes
+  // past the last line read the last line's parts and store nothing.
+  if (!live && pl == 1) return;
+  const int4 sp = a.split[w < nsplit ? w : nsplit - 1];
+  const float *q = a.partial + (int64_t)sp.z * BW + b0;  // b0 < BW
   float s[VEC];
 #pragma unroll
   for (int i = 0; i < VEC; ++i) s[i] = 0.f;
-  for (int p = 0; p < sp.y; p += 8) {
+  for (int p = j; p < sp.y; p += 8 * pl) {
     float x[8][VEC];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      // past the last part: load the last part again (no branch, so all
-      // eight loads issue together) and leave it out of the sum
-      const float *r = q + (int64_t)min(p + u, sp.y - 1) * BW;
+      const float *rp = q + (int64_t)min(p + u * pl, sp.y - 1) * BW;
       if constexpr (VEC == 4) {
-        const float4 f = __ldcg(reinterpret_cast<const float4 *>(r));
+        const float4 f = __ldcg(reinterpret_cast<const float4 *>(rp));
         x[u][0] = f.x;
         x[u][1] = f.y;
         x[u][2] = f.z;
         x[u][3] = f.w;
       } else {
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) x[u][i] = __ldcg(r + i);
+        for (int i = 0; i < VEC; ++i) x[u][i] = __ldcg(rp + i);
       }
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u)
-      if (p + u < sp.y) {
+      if (p + u * pl < sp.y) {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) s[i] += x[u][i];
       }
   }
-  float *d = a.dst + (int64_t)b0 * a.ld + line;
+  for (int off = TPL; off < tpl; off <<= 1)
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) s[i] += __shfl_xor_sync(0xffffffffu, s[i], off);
+  if (!live || j != 0) return;
+  float *d = a.dst + (int64_t)b0 * a.ld + a.seg[sp.x].x;
 #pragma unroll
   for (int i = 0; i < VEC; ++i)
     if (b0 + i < a.nb) d[(int64_t)i * a.ld] = s[i];

@@ -322,6 +322,7 @@ void build_segments(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz
   split.clear();
   t.mean_len = nlines > 0 ? (double)nnz / (double)nlines : 0.0;
   t.max_len = 0;
+  t.max_parts = 0;
   for (int64_t l = 0; l < nlines; ++l) t.max_len = std::max<int64_t>(t.max_len, ptr[l + 1] - ptr[l]);
   int64_t cap = std::max<int64_t>(256, 2 * (int64_t)std::ceil(t.mean_len));
   if ((double)t.max_len > 8.0 * t.mean_len)
@@ -337,6 +338,7 @@ void build_segments(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz
     const int sid = (int)split.size();
     split.push_back(make_int4((int)seg.size(), (int)parts, (int)slots, 0));
     slots += parts;
+    t.max_parts = std::max<int>(t.max_parts, (int)parts);
     for (int64_t p = 0; p < parts; ++p)
       seg.push_back(make_int4((int)l, (int)(b + p * len / parts), (int)(b + (p + 1) * len / parts),
                               sid));
@@ -354,6 +356,7 @@ void build_cut(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz, int
   split.clear();
   t.mean_len = nlines > 0 ? (double)nnz / (double)nlines : 0.0;
   t.max_len = 0;
+  t.max_parts = 0;
   int64_t slots = 0;
   for (int64_t l = 0; l < nlines; ++l) {
     const int64_t b = ptr[l], e = ptr[l + 1], len = e - b;
@@ -365,6 +368,7 @@ void build_cut(const std::vector<int32_t> &ptr, int64_t nlines, int64_t nnz, int
     const int sid = (int)split.size();
     split.push_back(make_int4((int)seg.size(), parts, (int)slots, 0));
     slots += parts;
+    t.max_parts = std::max(t.max_parts, parts);
     for (int q = 0; q < parts; ++q)
       seg.push_back(make_int4((int)l, (int)(b + q * len / parts), (int)(b + (q + 1) * len / parts),
                               sid));
