@@ -184,13 +184,15 @@ int sddmm_subranges(const snack::SegTable &t, const snack::Plan &p) {
 
 // Whether the split lines of an SpMM over table t with plan q are summed by
 // a second pass (split_sums) instead of by the last part's team: for slices
-// of 16+ floats, where the tickets' fences and the serial sum of the parts
-// sit on the kernel's critical path (10000 x 10000 at 95 %, halved lines,
-// batch 64 forward 91.1 -> 84.7 us; 8192 x 8192 Zipf rows, batch 16 20.8 ->
-// 20.1).  At narrower slices the extra launch costs what it saves (Zipf
-// rows, batch 1: 12.2 -> 12.4 us).
-bool two_pass(const snack::SegTable &t, const snack::Plan &q) {
-  return t.nsplit > 0 && q.bw >= 16;
+// of 8+ floats (16+ inside the fused backward), where the tickets' fences and
+// the serial sum of the parts sit on the kernel's critical path (10000 x
+// 10000 at 95 %, halved lines, batch 64 forward 91.1 -> 84.7 us; 8192 x 8192
+// Zipf rows forward, batch 16 20.8 -> 20.1, batch 8 18.5 -> 16.9).  At
+// narrower slices the extra launch costs what it saves (Zipf rows, batch 1:
+// forward 12.3 -> 12.8 us, fused backward 12.8 -> 14.4; batch 2 and 4 even),
+// and so does it in the fused backward at 8 (20.5 -> 21.0).
+bool two_pass(const snack::SegTable &t, const snack::Plan &q, bool fused = false) {
+  return t.nsplit > 0 && q.bw >= (fused ? 16 : 8);
 }
 
 // dX over the column segments: through the permutation, or (values in
@@ -384,7 +386,7 @@ snack_status run_backward_slice(snack_handle h, const float *X, const float *dY,
     return SNACK_OK;
   }
   if (dX && want_w) {
-    const bool two = two_pass(tc, pc);
+    const bool two = two_pass(tc, pc, true);
     if (two) cols.counter = nullptr;
     e = snack::launch_backward_fused(pc, cols, pr, rows, true, s);
     if (e == cudaSuccess && two) {
