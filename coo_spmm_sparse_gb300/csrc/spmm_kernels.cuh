@@ -598,8 +598,6 @@ __device__ __forceinline__ void load_col_step(const int32_t *col, int kb, int k1
   }
 }
 
-// dW for up to two quads of one group (columns already loaded): the G lanes
-// of a group each form part of the batch dot product and meet by shuffle.
 // dW of one quad when its four dot products are spread over a group of G
 // >= 2 lanes (d[e]: this lane's part of entry e): a butterfly over the
 // group sums them and leaves one entry per lane at once.  The first level
@@ -639,6 +637,12 @@ __device__ __forceinline__ void sddmm_store_spread(const SddmmArgs &a, int kq, i
   }
 }
 
+// dW for up to two quads of one group (columns already loaded): the G lanes
+// of a group each form part of the batch dot product.  SPREAD: the quad's
+// four sums meet in sddmm_store_spread; else each entry is summed over the
+// group by shuffles and one lane stores the quad (the fused backward at
+// slices of 64+ floats, where the butterfly measured slower) or applies the
+// optimizer step (OPT, whose update reads all four sums in one lane).
 template <int BW, bool SM, bool OPT, bool SPREAD>
 __device__ __forceinline__ void sddmm_quads(const SddmmArgs &a, const float *xt, int kb, int k0,
                                             int k1, int npt, unsigned gmask, int sub,
