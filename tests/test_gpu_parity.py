@@ -322,6 +322,19 @@ def test_heavy_tailed_rows_with_empty_rows():
         check_products(h, out, inp, ref2, Xb, dY, fused=False)
 
 
+def test_one_row_of_sixty_thousand_entries():
+    """A 64 x 60000 layer whose row 0 holds every column, beside rows of 0-30
+    entries: the heavy-tailed cut gives that row about 900 parts, so the
+    second pass's threads each walk many parts in several rounds of eight
+    loads (at every slice width from 8 floats), and the tickets sum them at
+    slices of 1-4."""
+    out, inp = 64, 60000
+    row, col, val = _heavy_tailed(out, inp, [0], seed=31)
+    h, ref = _layer_case(out, inp, row, col, val, [1, 3, 8, 16, 40, 64, 200], seed=32)
+    _, _, segs = sn().snack_plan(h, 0, 16)
+    assert segs > out + 500  # the full row alone is cut into hundreds of parts
+
+
 def test_halved_lines_wide_slices():
     # 2.2 M entries over 4096 x 4096 (537 per row and column): 64-wide
     # slices walk every line in four parts, 32-wide slices of the weight
