@@ -443,6 +443,10 @@ def run_ours(args):
                 "kernel": f"{dom['op']} {dom['shape']} nnz={dom['nnz']} B={dom['B']}",
                 "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
                 "bytes": "metric bytes nnz*12 + dense operands, per launch",
+                # the rate at which the op gathers operand rows (4 * B bytes per
+                # stored entry, through L1 from L2): from batch ~8 on, this and
+                # not DRAM is what the kernels' time follows
+                "gather_gbs": dom["gather_gbs"],
                 "at_95pct_batch_ge_8": target}
 
     # End to end through the same calls with host buffers: each step's inputs
