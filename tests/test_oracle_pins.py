@@ -392,6 +392,23 @@ def test_prune_regrow_invariants_and_count():
     assert kept >= nnz - 2 * res["pruned"]
 
 
+def test_prune_count_is_the_floor_of_the_float_fraction_times_nnz():
+    """P = floor(f * nnz) for the float32 f the call takes: the exact product
+    of the float's value and nnz (rational arithmetic here), so 0.7f * 10 is
+    6 (0.7f is just below 0.7) while 0.3f * 10 is 3; no pruning for f <= 0
+    or NaN, everything for f >= 1."""
+    from fractions import Fraction
+    for f in (0.3, 0.7, 0.05, 0.5, 0.25, 1e-7, 0.999999):
+        for nnz in (1, 10, 6554, 117965, 1_000_000, 10_000_000, (1 << 28) + 3):
+            want = math.floor(Fraction(float(np.float32(f))) * nnz)
+            assert oracle.prune_count(f, nnz) == want, (f, nnz)
+    assert oracle.prune_count(0.7, 10) == 6 and oracle.prune_count(0.3, 10) == 3
+    for f in (0.0, -0.5, float("nan")):
+        assert oracle.prune_count(f, 1000) == 0
+    for f in (1.0, 1.5, float("inf")):
+        assert oracle.prune_count(f, 1000) == 1000
+
+
 def test_prune_zero_fraction_is_identity():
     out, inp = 20, 20
     row, col = workloads.uniform_pattern(out, inp, 50, 1)
