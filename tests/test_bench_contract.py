@@ -58,6 +58,7 @@ def test_our_arm_line():
     assert r["achieved"] > 0 and r["peak"] > 0
     assert abs(r["frac"] - r["achieved"] / r["peak"]) <= 1e-3 * max(1.0, r["frac"])
     assert r["traffic"] is None or r["traffic"] > 0
+    assert r["gather_gbs"] > 0
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
     assert cb["all_cores"]["cores"] >= 1 and cb["all_cores"]["value"] > 0
@@ -67,5 +68,7 @@ def test_our_arm_line():
     # the end-to-end number moves real bytes and is not the device-timed value
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
     assert d["e2e"]["value"] != d["value"]
+    lo, mid, hi = d["e2e"]["ms_per_step_min_median_max"]
+    assert 0 < lo <= mid <= hi
     for o in d["ops"]:
         assert o["us"] > 0 and o["us_median"] > 0 and o["gather_gbs"] > 0
